@@ -1,0 +1,33 @@
+"""Plain fp64 CPU oracle for exact softmax attention.
+
+TEST INFRASTRUCTURE ONLY.  Only the test suite, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import or run anything in this package.  The
+product path (the CUDA library and its Python binding) never imports it, and this
+package imports nothing from the product path.
+
+Every function is written from the pages' statement of the method, in float64,
+materialising the score matrix S and the probability matrix P on purpose:
+
+* ``attn_fwd_ref``  -- the plain definition O = softmax(scale*Q*K^T) * V and the
+  per-row log-sum-exp.
+* ``attn_bwd_ref``  -- the textbook gradient of that definition (the pages say only
+  that the backward recomputes S and P from Q, K and the saved statistics; the
+  formulas are the derivative of the definition above).
+* ``online_softmax_stats`` / ``online_attention_row`` / ``attn_fwd_tiled_ref`` --
+  the streaming (m, l) recurrence, used only to check the oracle's own algebra.
+
+Parity pins: every function here is pinned by tests in ``tests/test_oracle_pins.py``
+against printed worked examples, closed forms, invariants, library routines and
+central finite differences.  No function is "parity unpinned".
+"""
+
+from .attention import (  # noqa: F401
+    softmax_two_pass,
+    online_softmax_stats,
+    online_attention_row,
+    attn_fwd_ref,
+    attn_fwd_tiled_ref,
+    attn_bwd_ref,
+    attn_head_fwd,
+    attn_head_bwd,
+)
