@@ -1,0 +1,184 @@
+"""Python binding of the C ABI in include/fa.h: argument marshalling only.
+
+Every step of the attention computation runs in the CUDA kernels of
+``lib/libfa_gb300.so``; this module checks torch tensors, passes their device
+pointers and the current CUDA stream to the library, and turns status codes into
+exceptions.  There is no fallback: if the library is missing or the device is not an
+sm_100-family GPU, the call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "lib", "libfa_gb300.so")
+
+FA_BF16, FA_FP16 = 0, 1
+STATUS = {
+    0: "FA_OK", 1: "FA_ERR_NULL", 2: "FA_ERR_SHAPE", 3: "FA_ERR_UNSUPPORTED_D", 4: "FA_ERR_DTYPE",
+    5: "FA_ERR_ALIGN", 6: "FA_ERR_WORKSPACE", 7: "FA_ERR_LAUNCH", 8: "FA_ERR_DEVICE_TIMEOUT",
+    9: "FA_ERR_NO_DEVICE", 10: "FA_ERR_SCALE",
+}
+STATUS_CODE = {v: k for k, v in STATUS.items()}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({strerror(status)})")
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"CUDA library not found at {p}; build it with "
+                "`python -m exact_tiled_attention_27_gb300.build`")
+        lib = ctypes.CDLL(p)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
+        lib.fa_fwd.restype = i
+        lib.fa_bwd_workspace_size.argtypes = [i, i, i, i]
+        lib.fa_bwd_workspace_size.restype = sz
+        lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, f, i, i, vp]
+        lib.fa_bwd.restype = i
+        lib.fa_strerror.argtypes = [i]
+        lib.fa_strerror.restype = ctypes.c_char_p
+        lib.fa_get_last_kernel_status.argtypes = [vp]
+        lib.fa_get_last_kernel_status.restype = i
+        lib.fa_device_sm_count.argtypes = []
+        lib.fa_device_sm_count.restype = i
+        lib.fa_debug_wait_timeout.argtypes = [ctypes.c_uint, vp]
+        lib.fa_debug_wait_timeout.restype = i
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def strerror(status: int) -> str:
+    try:
+        return load_library().fa_strerror(int(status)).decode()
+    except Exception:  # library missing: still give the symbolic name
+        return STATUS.get(int(status), "unknown")
+
+
+# ----------------------------------------------------------------------------- torch glue
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t):
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return FA_BF16
+    if t.dtype == torch.float16:
+        return FA_FP16
+    raise TypeError(f"expected bfloat16 or float16 tensors, got {t.dtype}")
+
+
+def _check_bhnd(name, t, shape, dtype):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (batch, heads, seq, head_dim)")
+
+
+def _stream_handle(stream=None):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def workspace_size(B, H, N, d) -> int:
+    return int(load_library().fa_bwd_workspace_size(B, H, N, d))
+
+
+def forward(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None):
+    """Exact attention forward.  q, k, v: (B, H, N, d) bf16/fp16 CUDA tensors.
+
+    Returns (o, lse): o like q, lse float32 (B, H, N), natural-log row log-sum-exp
+    of scale * q k^T.  ``scale`` defaults to d ** -0.5.  Runs on the current stream.
+    """
+    torch = _torch()
+    B, H, N, d = q.shape
+    _check_bhnd("q", q, (B, H, N, d), q.dtype)
+    _check_bhnd("k", k, (B, H, N, d), q.dtype)
+    _check_bhnd("v", v, (B, H, N, d), q.dtype)
+    scale = float(d) ** -0.5 if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check_bhnd("out", out, (B, H, N, d), q.dtype)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 (B, H, N) tensor")
+    st = load_library().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d, scale,
+                               1 if causal else 0, _dtype_code(q), _stream_handle(stream))
+    if st != 0:
+        raise FaError(st, "fa_fwd")
+    return out, lse
+
+
+def backward(q, k, v, o, do, lse, scale=None, causal=False, dq=None, dk=None, dv=None, workspace=None,
+             stream=None):
+    """Exact attention backward.  Returns (dq, dk, dv) like q.
+
+    ``workspace`` (optional) is a CUDA uint8 tensor of at least workspace_size(B,H,N,d)
+    bytes; one is allocated through torch when it is not given.
+    """
+    torch = _torch()
+    B, H, N, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
+        _check_bhnd(name, t, (B, H, N, d), q.dtype)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 (B, H, N) tensor")
+    scale = float(d) ** -0.5 if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_bhnd(name, t, (B, H, N, d), q.dtype)
+    need = workspace_size(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace too small: need {need} bytes")
+    st = load_library().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
+                               _ptr(dv), _ptr(workspace), need, B, H, N, d, scale, 1 if causal else 0,
+                               _dtype_code(q), _stream_handle(stream))
+    if st != 0:
+        raise FaError(st, "fa_bwd")
+    return dq, dk, dv
+
+
+def last_kernel_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error status."""
+    return int(load_library().fa_get_last_kernel_status(_stream_handle(stream)))
+
+
+def device_sm_count() -> int:
+    return int(load_library().fa_device_sm_count())
+
+
+def debug_wait_timeout(limit_us: int, stream=None) -> int:
+    return int(load_library().fa_debug_wait_timeout(int(limit_us), _stream_handle(stream)))

@@ -1,0 +1,277 @@
+// api.cu -- the C ABI declared in include/fa.h: argument validation, tensor-map
+// encoding, workspace carving, launches and the device error word.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fa.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+// One error word per device: bit 31 set by a kernel whose bounded wait gave up.
+__device__ unsigned int g_err_word;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  int num_sms = 0;
+  int major = 0;
+  unsigned int* err_word = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int get_device(DeviceInfo** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return FA_ERR_NO_DEVICE;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return FA_ERR_NO_DEVICE;
+    }
+    if (prop.major != 10) return FA_ERR_NO_DEVICE;   // tcgen05 / TMEM need the sm_100 family
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) {
+      cudaGetLastError();
+      return FA_ERR_NO_DEVICE;
+    }
+    if (g_encode == nullptr) {
+      cudaDriverEntryPointQueryResult q;
+      void* fn = nullptr;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr) {
+        cudaGetLastError();
+        return FA_ERR_NO_DEVICE;
+      }
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    d.num_sms = prop.multiProcessorCount;
+    d.major = prop.major;
+    d.err_word = static_cast<unsigned int*>(p);
+    d.ready = true;
+  }
+  *out = &d;
+  return FA_OK;
+}
+
+// 3-D map over a contiguous (B*H, N, d) 16-bit tensor: box of 128 rows x 64 elements
+// (one 128-byte swizzle row per tensor row); rows past N read as zero.
+bool encode_bhnd(CUtensorMap* m, const void* base, int BH, int N, int d, int dtype) {
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(m, dtype == FA_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                              3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_common(int B, int H, int N, int d, float scale, int dtype) {
+  if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_DTYPE;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED_D;
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
+  const long long bhn = (long long)B * H * N;
+  if ((long long)B * H > (1LL << 30) || bhn >= (1LL << 31) || bhn * d >= (1LL << 40)) return FA_ERR_SHAPE;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_SCALE;
+  return FA_OK;
+}
+
+constexpr size_t kAlign = 256;
+size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct WsLayout {
+  size_t dvec_off, lse2_off, acc_off, total;
+  int Npad;
+};
+
+WsLayout ws_layout(int B, int H, int N, int d) {
+  WsLayout w;
+  w.Npad = (N + 127) / 128 * 128;
+  const size_t rows = (size_t)B * H * w.Npad;
+  w.dvec_off = 0;
+  w.lse2_off = round_up(rows * 4);
+  w.acc_off = w.lse2_off + round_up(rows * 4);
+  w.total = w.acc_off + round_up((size_t)B * H * N * d * 4);
+  return w;
+}
+
+// Test hook: wait on an mbarrier nobody arrives on, give up after the limit.
+__global__ void debug_wait_kernel(unsigned int* err_word, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const WaitCtl ctl{&abort_flag, err_word, limit_ns};
+  mbar_wait(smem_u32(&bar), 0, ctl, 0x7ff);
+  __syncthreads();
+}
+
+}  // namespace
+
+cudaError_t launch_debug_wait(unsigned int* err_word, uint64_t limit_ns, cudaStream_t stream) {
+  debug_wait_kernel<<<1, 32, 0, stream>>>(err_word, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d, float scale,
+           int causal, int dtype, void* stream) {
+  int st = check_common(B, H, N, d, scale, dtype);
+  if (st != FA_OK) return st;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return FA_ERR_ALIGN;
+  DeviceInfo* dev = nullptr;
+  st = get_device(&dev);
+  if (st != FA_OK) return st;
+  FwdArgs a;
+  const int BH = B * H;
+  if (!encode_bhnd(&a.tm_q, q, BH, N, d, dtype) || !encode_bhnd(&a.tm_k, k, BH, N, d, dtype) ||
+      !encode_bhnd(&a.tm_v, v, BH, N, d, dtype))
+    return FA_ERR_LAUNCH;
+  a.o = o;
+  a.lse = lse;
+  a.BH = BH;
+  a.N = N;
+  a.d = d;
+  a.dtype = dtype;
+  a.causal = causal ? 1 : 0;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.err_word = dev->err_word;
+  a.limit_ns = kWaitLimitNs;
+  a.num_sms = dev->num_sms;
+  return launch_fwd(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
+  if (check_common(B, H, N, d, 1.0f, FA_BF16) != FA_OK) return 0;
+  return ws_layout(B, H, N, d).total;
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse, void* dq,
+           void* dk, void* dv, void* workspace, size_t ws_bytes, int B, int H, int N, int d, float scale, int causal,
+           int dtype, void* stream) {
+  int st = check_common(B, H, N, d, scale, dtype);
+  if (st != FA_OK) return st;
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) || !aligned16(dq) ||
+      !aligned16(dk) || !aligned16(dv) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return FA_ERR_ALIGN;
+  const WsLayout w = ws_layout(B, H, N, d);
+  if (workspace == nullptr || ws_bytes < w.total || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
+    return FA_ERR_WORKSPACE;
+  DeviceInfo* dev = nullptr;
+  st = get_device(&dev);
+  if (st != FA_OK) return st;
+  BwdArgs a;
+  const int BH = B * H;
+  if (!encode_bhnd(&a.tm_q, q, BH, N, d, dtype) || !encode_bhnd(&a.tm_k, k, BH, N, d, dtype) ||
+      !encode_bhnd(&a.tm_v, v, BH, N, d, dtype) || !encode_bhnd(&a.tm_do, dO, BH, N, d, dtype))
+    return FA_ERR_LAUNCH;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.o = o;
+  a.dO = dO;
+  a.lse = lse;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.dvec = reinterpret_cast<float*>(ws + w.dvec_off);
+  a.lse2 = reinterpret_cast<float*>(ws + w.lse2_off);
+  a.dq_accum = reinterpret_cast<float*>(ws + w.acc_off);
+  a.BH = BH;
+  a.N = N;
+  a.Npad = w.Npad;
+  a.d = d;
+  a.dtype = dtype;
+  a.causal = causal ? 1 : 0;
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.err_word = dev->err_word;
+  a.limit_ns = kWaitLimitNs;
+  a.num_sms = dev->num_sms;
+  return launch_bwd(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+const char* fa_strerror(int status) {
+  switch (status) {
+    case FA_OK: return "ok";
+    case FA_ERR_NULL: return "a required pointer is NULL";
+    case FA_ERR_SHAPE: return "B, H and N must be >= 1 and B*H*N < 2^31";
+    case FA_ERR_UNSUPPORTED_D: return "head_dim must be 64 or 128";
+    case FA_ERR_DTYPE: return "dtype must be FA_BF16 or FA_FP16";
+    case FA_ERR_ALIGN: return "tensor base addresses must be 16-byte aligned (lse: 4-byte)";
+    case FA_ERR_WORKSPACE: return "workspace missing, misaligned (256 bytes) or smaller than fa_bwd_workspace_size";
+    case FA_ERR_LAUNCH: return "the CUDA runtime rejected a launch";
+    case FA_ERR_DEVICE_TIMEOUT: return "a kernel's bounded pipeline wait gave up";
+    case FA_ERR_NO_DEVICE: return "no usable sm_100-family CUDA device is current";
+    case FA_ERR_SCALE: return "scale must be finite and > 0";
+    default: return "unknown status";
+  }
+}
+
+int fa_get_last_kernel_status(void* stream) {
+  DeviceInfo* dev = nullptr;
+  int st = get_device(&dev);
+  if (st != FA_OK) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_LAUNCH;
+  }
+  unsigned int word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_err_word, sizeof(word)) != cudaSuccess) return FA_ERR_LAUNCH;
+  if (word != 0) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_err_word, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_LAUNCH;
+  }
+  return (word & kErrTimeoutBit) ? FA_ERR_DEVICE_TIMEOUT : FA_OK;
+}
+
+int fa_device_sm_count(void) {
+  DeviceInfo* dev = nullptr;
+  const int st = get_device(&dev);
+  return st == FA_OK ? dev->num_sms : -st;
+}
+
+int fa_debug_wait_timeout(unsigned limit_us, void* stream) {
+  DeviceInfo* dev = nullptr;
+  const int st = get_device(&dev);
+  if (st != FA_OK) return st;
+  if (limit_us < 1) limit_us = 1;
+  if (limit_us > 2000000) limit_us = 2000000;
+  return launch_debug_wait(dev->err_word, (uint64_t)limit_us * 1000ull, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? FA_OK
+             : FA_ERR_LAUNCH;
+}
+
+}  // extern "C"

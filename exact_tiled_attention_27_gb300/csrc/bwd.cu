@@ -1,0 +1,546 @@
+// bwd.cu -- backward kernels of exact tiled attention for sm_103a.
+//
+// The backward recomputes the probabilities on chip from Q, K and the saved row
+// log-sum-exp instead of reading a stored N x N matrix (review of the FlashAttention
+// paper, "方法细节"; "Flash Attention" chapter, end of "FlashAttention——把整件事分块
+// 塞进 SRAM").  Gradient formulas are the derivative of O = softmax(scale Q K^T) V:
+//
+//   dV = P^T dO,  dP = dO V^T,  D_i = sum_c dO_ic O_ic,  dS = P o (dP - D),
+//   dQ = scale dS K,  dK = scale dS^T Q.
+//
+// Three launches:
+//   bwd_pre_kernel   D and lse*log2(e) per row, padded to whole 128-row blocks
+//                    (padding rows get D = 0 and +inf, so their P is exactly 0);
+//                    zeroes the float32 dQ accumulator.
+//   bwd_kv_kernel    persistent over (batch*head, 128-key block) tiles, key/value
+//                    block on the outside, query blocks inside.  Per query block:
+//                      S^T = K Q^T, dP^T = V dO^T            (tcgen05, tensor memory)
+//                      P^T = 2^(S^T scale log2e - lse2), dS^T = P^T o (dP^T - D)
+//                                                            (one thread per key row)
+//                      dV += P^T dO, dK += dS^T Q, dQ_part = dS K
+//                    dQ_part is added into the float32 accumulator with vector
+//                    reductions; dK (times scale) and dV are written once per tile.
+//   bwd_dq_kernel    dq = scale * accumulator, rounded to the 16-bit type.
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kRows = 128;
+constexpr int kChunkBytes = kRows * 128;
+constexpr int kBwdThreads = 320;   // ds warpgroup (0-3), dQ warpgroup (4-7), producer (8), MMA (9)
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kTileBytes = kRows * D * 2;
+  static constexpr int kKVBufs = (D == 64) ? 2 : 1;
+  static constexpr int kQBufs = (D == 64) ? 2 : 1;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kKVBufs * kTileBytes;
+  static constexpr int kOffQ = kOffV + kKVBufs * kTileBytes;
+  static constexpr int kOffDO = kOffQ + kQBufs * kTileBytes;
+  static constexpr int kOffPT = kOffDO + kQBufs * kTileBytes;        // 128 x 128 16-bit, K-major SW128
+  static constexpr int kOffDST = kOffPT + 2 * kChunkBytes;           // 128 x 128 16-bit, K-major SW128
+  static constexpr int kOffStats = kOffDST + 2 * kChunkBytes;        // [kQBufs][2][128] float
+  static constexpr int kOffBar = kOffStats + kQBufs * 2 * kRows * 4;
+  // barriers
+  static constexpr int kKVFull = 0;                   // [kKVBufs]
+  static constexpr int kKVEmpty = kKVFull + kKVBufs;  // [kKVBufs]
+  static constexpr int kQFull = kKVEmpty + kKVBufs;   // [kQBufs]
+  static constexpr int kQEmpty = kQFull + kQBufs;     // [kQBufs]
+  static constexpr int kSFull = kQEmpty + kQBufs;
+  static constexpr int kDSFull = kSFull + 1;
+  static constexpr int kMmaDone = kDSFull + 1;
+  static constexpr int kDQFull = kMmaDone + 1;
+  static constexpr int kDQFree = kDQFull + 1;
+  static constexpr int kDKVFull = kDQFree + 1;
+  static constexpr int kDKVEmpty = kDKVFull + 1;
+  static constexpr int kDrain = kDKVEmpty + 1;
+  static constexpr int kNumBars = kDrain + 1;
+  static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
+  // tensor memory columns (512 allocated)
+  static constexpr uint32_t kTmST = 0;
+  static constexpr uint32_t kTmDPT = 128;
+  static constexpr uint32_t kTmDV = 256;
+  static constexpr uint32_t kTmDK = 256 + D;
+  static constexpr uint32_t kTmDQ = (D == 64) ? 384 : 0;   // d = 128 reuses the S^T columns
+};
+
+__device__ __forceinline__ void decode_kv_tile(int tile, int BH, int nkb, int causal, int& bh, int& kb) {
+  // Causal: key block kb has nkb - kb query blocks; lightest-last order puts kb = 0 first.
+  (void)nkb;
+  (void)causal;
+  const int r = tile / BH;
+  bh = tile - r * BH;
+  kb = r;
+}
+
+// 16-byte unit `u` (8 elements) of row `r` inside a 128-row x 128-byte swizzled block.
+__device__ __forceinline__ uint32_t sw128_offset(int r, int u) {
+  return static_cast<uint32_t>(r * 128 + ((u ^ (r & 7)) << 4));
+}
+
+template <int D, int DT, bool CAUSAL>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  const float* __restrict__ lse2, const float* __restrict__ dvec, float* __restrict__ dq_accum,
+                  uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, int BH, int N, int Npad, float scale,
+                  float scale_log2, unsigned int* err_word, uint64_t limit_ns) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int nb = (N + kRows - 1) / kRows;
+  const int ntiles = BH * nb;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kKVBufs; ++i) {
+      mbar_init(bar(C::kKVFull + i), 1);
+      mbar_init(bar(C::kKVEmpty + i), 1);
+    }
+    for (int i = 0; i < C::kQBufs; ++i) {
+      mbar_init(bar(C::kQFull + i), 1);
+      mbar_init(bar(C::kQEmpty + i), 1);
+    }
+    mbar_init(bar(C::kSFull), 1);
+    mbar_init(bar(C::kDSFull), kRows);
+    mbar_init(bar(C::kMmaDone), 1);
+    mbar_init(bar(C::kDQFull), 1);
+    mbar_init(bar(C::kDQFree), kRows);
+    mbar_init(bar(C::kDKVFull), 1);
+    mbar_init(bar(C::kDKVEmpty), kRows);
+    mbar_init(bar(C::kDrain), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_holder), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const WaitCtl ctl{abort_flag, err_word, limit_ns};
+  const WaitCtl drain{nullptr, err_word, limit_ns};
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      prefetch_tmap(&tm_do);
+      uint32_t s = 0;
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++it) {
+        int bh, kb;
+        decode_kv_tile(tile, BH, nb, CAUSAL, bh, kb);
+        const int kvb = it % C::kKVBufs;
+        if (it >= C::kKVBufs &&
+            !mbar_wait(bar(C::kKVEmpty + kvb), ((it / C::kKVBufs) - 1) & 1, ctl, 0x401)) {
+          ok = false;
+          break;
+        }
+        const uint32_t kdst = smem_u32(smem + C::kOffK + kvb * C::kTileBytes);
+        const uint32_t vdst = smem_u32(smem + C::kOffV + kvb * C::kTileBytes);
+        mbar_arrive_expect_tx(bar(C::kKVFull + kvb), 2 * C::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c) {
+          tma_load_3d(kdst + c * kChunkBytes, &tm_k, bar(C::kKVFull + kvb), c * 64, kb * kRows, bh);
+          tma_load_3d(vdst + c * kChunkBytes, &tm_v, bar(C::kKVFull + kvb), c * 64, kb * kRows, bh);
+        }
+        const int q0 = CAUSAL ? kb : 0;
+        for (int qi = q0; qi < nb; ++qi, ++s) {
+          const int qs = s % C::kQBufs;
+          if (s >= (uint32_t)C::kQBufs &&
+              !mbar_wait(bar(C::kQEmpty + qs), ((s / C::kQBufs) - 1) & 1, ctl, 0x402)) {
+            ok = false;
+            break;
+          }
+          const uint32_t qdst = smem_u32(smem + C::kOffQ + qs * C::kTileBytes);
+          const uint32_t odst = smem_u32(smem + C::kOffDO + qs * C::kTileBytes);
+          const uint32_t stats = smem_u32(smem + C::kOffStats + qs * 2 * kRows * 4);
+          mbar_arrive_expect_tx(bar(C::kQFull + qs), 2 * C::kTileBytes + 2 * kRows * 4);
+#pragma unroll
+          for (int c = 0; c < C::kChunks; ++c) {
+            tma_load_3d(qdst + c * kChunkBytes, &tm_q, bar(C::kQFull + qs), c * 64, qi * kRows, bh);
+            tma_load_3d(odst + c * kChunkBytes, &tm_do, bar(C::kQFull + qs), c * 64, qi * kRows, bh);
+          }
+          const size_t srow = (size_t)bh * Npad + (size_t)qi * kRows;
+          bulk_load(stats, lse2 + srow, kRows * 4, bar(C::kQFull + qs));
+          bulk_load(stats + kRows * 4, dvec + srow, kRows * 4, bar(C::kQFull + qs));
+        }
+      }
+      if (!ok) {
+        // let every copy already issued land before the CTA exits
+        for (int b = 0; b < C::kKVBufs; ++b)
+          if (it > b) {
+            const int last = it - 1 - ((it - 1 - b) % C::kKVBufs);
+            mbar_wait(bar(C::kKVFull + b), (last / C::kKVBufs) & 1, drain, 0x4f1);
+          }
+        for (int b = 0; b < C::kQBufs; ++b)
+          if (s > (uint32_t)b) {
+            const uint32_t last = s - 1 - ((s - 1 - b) % C::kQBufs);
+            mbar_wait(bar(C::kQFull + b), (last / C::kQBufs) & 1, drain, 0x4f2);
+          }
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t ab = (DT == 0) ? 1u : 0u;
+      constexpr uint32_t idesc_s = idesc_f16(ab, 0, 0, 128, 128);    // A, B K-major
+      constexpr uint32_t idesc_kv = idesc_f16(ab, 0, 1, 128, D);     // A K-major, B MN-major
+      constexpr uint32_t idesc_q = idesc_f16(ab, 1, 1, 128, D);      // A MN-major, B MN-major
+      const uint32_t pt = smem_u32(smem + C::kOffPT);
+      const uint32_t dst = smem_u32(smem + C::kOffDST);
+      uint32_t s = 0;
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++it) {
+        int bh, kb;
+        decode_kv_tile(tile, BH, nb, CAUSAL, bh, kb);
+        const int kvb = it % C::kKVBufs;
+        if (!mbar_wait(bar(C::kKVFull + kvb), (it / C::kKVBufs) & 1, ctl, 0x501)) break;
+        const uint32_t kbase = smem_u32(smem + C::kOffK + kvb * C::kTileBytes);
+        const uint32_t vbase = smem_u32(smem + C::kOffV + kvb * C::kTileBytes);
+        const int q0 = CAUSAL ? kb : 0;
+        for (int qi = q0; qi < nb; ++qi, ++s) {
+          const int qs = s % C::kQBufs;
+          if (!mbar_wait(bar(C::kQFull + qs), (s / C::kQBufs) & 1, ctl, 0x502)) {
+            ok = false;
+            break;
+          }
+          // the dQ columns (and, at d = 128, the S^T columns they share) must be drained
+          if (s > 0 && !mbar_wait(bar(C::kDQFree), (s - 1) & 1, ctl, 0x503)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t qbase = smem_u32(smem + C::kOffQ + qs * C::kTileBytes);
+          const uint32_t obase = smem_u32(smem + C::kOffDO + qs * C::kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+            umma_ss(tmem + C::kTmST, sdesc_sw128(kbase + off, 16, 1024), sdesc_sw128(qbase + off, 16, 1024),
+                    idesc_s, kk > 0 ? 1u : 0u);
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+            umma_ss(tmem + C::kTmDPT, sdesc_sw128(vbase + off, 16, 1024), sdesc_sw128(obase + off, 16, 1024),
+                    idesc_s, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(bar(C::kSFull));
+          if (!mbar_wait(bar(C::kDSFull), s & 1, ctl, 0x504)) {
+            ok = false;
+            break;
+          }
+          if (qi == q0 && it > 0 && !mbar_wait(bar(C::kDKVEmpty), (it - 1) & 1, ctl, 0x505)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t first = (qi == q0) ? 1u : 0u;
+#pragma unroll
+          for (int kk = 0; kk < kRows / 16; ++kk) {
+            // A = P^T / dS^T (keys x q, q contiguous): K-major, 16 q = 32 bytes
+            const uint32_t aoff = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+            // B = dO / Q (q x d, d contiguous): MN-major, 16 q = 16 rows of 128 bytes
+            const uint32_t boff = kk * 16 * 128;
+            const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+            umma_ss(tmem + C::kTmDV, sdesc_sw128(pt + aoff, 16, 1024), sdesc_sw128(obase + boff, kChunkBytes, 1024),
+                    idesc_kv, acc);
+            umma_ss(tmem + C::kTmDK, sdesc_sw128(dst + aoff, 16, 1024), sdesc_sw128(qbase + boff, kChunkBytes, 1024),
+                    idesc_kv, acc);
+          }
+#pragma unroll
+          for (int kk = 0; kk < kRows / 16; ++kk) {
+            // A = dS (q x keys) read from the dS^T block: MN-major, 16 keys = 16 rows
+            // B = K (keys x d, d contiguous): MN-major, 16 keys = 16 rows
+            const uint32_t off = kk * 16 * 128;
+            umma_ss(tmem + C::kTmDQ, sdesc_sw128(dst + off, kChunkBytes, 1024),
+                    sdesc_sw128(kbase + off, kChunkBytes, 1024), idesc_q, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(bar(C::kMmaDone));
+          umma_commit(bar(C::kQEmpty + qs));
+          umma_commit(bar(C::kDQFull));
+        }
+        if (!ok) break;
+        umma_commit(bar(C::kKVEmpty + kvb));
+        umma_commit(bar(C::kDKVFull));
+      }
+      umma_commit(bar(C::kDrain));
+      mbar_wait(bar(C::kDrain), 0, drain, 0x5f1);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ dS warpgroup (one key row per thread)
+    const int t = threadIdx.x;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    uint8_t* pt = smem + C::kOffPT;
+    uint8_t* dst = smem + C::kOffDST;
+    uint32_t s = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+      int bh, kb;
+      decode_kv_tile(tile, BH, nb, CAUSAL, bh, kb);
+      const int key = kb * kRows + t;
+      const int q0 = CAUSAL ? kb : 0;
+      bool ok = true;
+      for (int qi = q0; qi < nb; ++qi, ++s) {
+        const int qs = s % C::kQBufs;
+        bool w = mbar_wait(bar(C::kSFull), s & 1, ctl, 0x601);
+        w = w && mbar_wait(bar(C::kQFull + qs), (s / C::kQBufs) & 1, ctl, 0x602);
+        w = w && (s == 0 || mbar_wait(bar(C::kMmaDone), (s - 1) & 1, ctl, 0x603));
+        if (!__all_sync(0xffffffffu, w)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float* st_lse2 = reinterpret_cast<const float*>(smem + C::kOffStats + qs * 2 * kRows * 4);
+        const float* st_d = st_lse2 + kRows;
+        const bool diag = CAUSAL && (qi == kb);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {   // 16 query columns per chunk
+          uint32_t sr[16], pr[16];
+          tmem_ld16(tmem + lane_base + C::kTmST + c * 16, sr);
+          tmem_ld16(tmem + lane_base + C::kTmDPT + c * 16, pr);
+          tmem_ld_wait();
+          reg_fence<16>(sr);
+          reg_fence<16>(pr);
+          uint32_t pw[8], dw[8];
+#pragma unroll
+          for (int e = 0; e < 16; e += 2) {
+            float p2[2], d2[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int col = c * 16 + e + h;
+              float p = ex2_approx(fmaf(__uint_as_float(sr[e + h]), scale_log2, -st_lse2[col]));
+              if (diag && (qi * kRows + col) < key) p = 0.f;
+              p2[h] = p;
+              d2[h] = p * (__uint_as_float(pr[e + h]) - st_d[col]);
+            }
+            pw[e >> 1] = pack2<DT>(p2[0], p2[1]);
+            dw[e >> 1] = pack2<DT>(d2[0], d2[1]);
+          }
+          // columns c*16 .. c*16+15 = 16-byte units 2c, 2c+1 of chunk (c / 4)
+          const int chunk = c >> 2;
+          const int u0 = (c & 3) * 2;
+          uint8_t* prow = pt + chunk * kChunkBytes;
+          uint8_t* drow = dst + chunk * kChunkBytes;
+          *reinterpret_cast<uint4*>(prow + sw128_offset(t, u0)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+          *reinterpret_cast<uint4*>(prow + sw128_offset(t, u0 + 1)) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
+          *reinterpret_cast<uint4*>(drow + sw128_offset(t, u0)) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
+          *reinterpret_cast<uint4*>(drow + sw128_offset(t, u0 + 1)) = make_uint4(dw[4], dw[5], dw[6], dw[7]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(C::kDSFull));
+      }
+      if (!ok) break;
+    }
+  } else {
+    // ------------------------------------------------------------ dQ warpgroup: dQ reduction, dK/dV epilogue
+    const int u = threadIdx.x - 128;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    uint32_t s = 0;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+      int bh, kb;
+      decode_kv_tile(tile, BH, nb, CAUSAL, bh, kb);
+      const int q0 = CAUSAL ? kb : 0;
+      bool ok = true;
+      for (int qi = q0; qi < nb; ++qi, ++s) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kDQFull), s & 1, ctl, 0x701))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t r[D];
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) tmem_ld32(tmem + lane_base + C::kTmDQ + c * 32, r + c * 32);
+        tmem_ld_wait();
+        reg_fence<D>(r);
+        tc_fence_before();
+        mbar_arrive(bar(C::kDQFree));
+        const int q = qi * kRows + u;
+        if (q < N) {
+          float* dst_row = dq_accum + ((size_t)bh * N + q) * D;
+#pragma unroll
+          for (int i = 0; i < D; i += 4)
+            red_add_v4(dst_row + i, __uint_as_float(r[i]), __uint_as_float(r[i + 1]), __uint_as_float(r[i + 2]),
+                       __uint_as_float(r[i + 3]));
+        }
+      }
+      if (!ok) break;
+      // dK, dV of this key block
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kDKVFull), it & 1, ctl, 0x702))) break;
+      tc_fence_after();
+      const int key = kb * kRows + u;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col0 = which == 0 ? C::kTmDV : C::kTmDK;
+        const float mul = which == 0 ? 1.0f : scale;
+        uint8_t* grow = reinterpret_cast<uint8_t*>(which == 0 ? dv : dk) + ((size_t)bh * N + key) * (D * 2);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_base + col0 + c * 32, r);
+          tmem_ld_wait();
+          reg_fence<32>(r);
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack2<DT>(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
+          if (key < N) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              st_global_v4(grow + c * 64 + i * 16, w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(C::kDKVEmpty));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// D = rowsum(dO o O) and lse2 = lse*log2(e) per row, padded rows -> (0, +inf);
+// also zeroes the float32 dQ accumulator.  8 threads per row for d = 64 (16 for
+// d = 128), each reading 16 bytes of O and of dO.
+template <int D, int DT>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
+                                                      const float* __restrict__ lse, float* __restrict__ dvec,
+                                                      float* __restrict__ lse2, float* __restrict__ dq_accum, int BH,
+                                                      int N, int Npad, size_t accum_elems) {
+  constexpr int kTPR = D / 8;   // threads per row
+  const long long gtid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long row = gtid / kTPR;  // padded row index over BH*Npad
+  const int part = (int)(gtid % kTPR);
+  const long long rows = (long long)BH * Npad;
+  const int bh = (int)(row / Npad);
+  const int n = (int)(row - (long long)bh * Npad);
+  float acc = 0.f;
+  const bool valid = (row < rows) && (n < N);
+  if (valid) {
+    const size_t base = ((size_t)bh * N + n) * D + part * 8;
+    const uint4 a = *reinterpret_cast<const uint4*>(o + base);
+    const uint4 b = *reinterpret_cast<const uint4*>(dout + base);
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+    const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 fa = unpack2<DT>(aw[i]);
+      const float2 fb = unpack2<DT>(bw[i]);
+      acc = fmaf(fa.x, fb.x, acc);
+      acc = fmaf(fa.y, fb.y, acc);
+    }
+  }
+#pragma unroll
+  for (int off = kTPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (part == 0 && row < rows) {
+    dvec[row] = valid ? acc : 0.f;
+    lse2[row] = valid ? lse[(size_t)bh * N + n] * kLog2e : INFINITY;
+  }
+  // zero the accumulator (grid-stride, 16 bytes per thread per step)
+  const size_t n4 = accum_elems / 4;
+  for (size_t i = (size_t)gtid; i < n4; i += (size_t)gridDim.x * blockDim.x)
+    reinterpret_cast<float4*>(dq_accum)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// dq = scale * dq_accum, rounded to the 16-bit type; 8 elements per thread.
+template <int DT>
+__global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ acc, uint16_t* __restrict__ dq,
+                                                     float scale, size_t n8) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+    const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
+    const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+    uint4 w;
+    w.x = pack2<DT>(a.x * scale, a.y * scale);
+    w.y = pack2<DT>(a.z * scale, a.w * scale);
+    w.z = pack2<DT>(b.x * scale, b.y * scale);
+    w.w = pack2<DT>(b.z * scale, b.w * scale);
+    reinterpret_cast<uint4*>(dq)[i] = w;
+  }
+}
+
+template <int D, int DT, bool CAUSAL>
+cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  // 1. preprocess
+  {
+    constexpr int kTPR = D / 8;
+    const long long threads = (long long)a.BH * a.Npad * kTPR;
+    long long blocks = (threads + 255) / 256;
+    const long long min_blocks = 4LL * a.num_sms;   // enough blocks to zero the accumulator quickly
+    if (blocks < min_blocks) blocks = min_blocks;
+    const size_t accum_elems = (size_t)a.BH * a.N * D;
+    bwd_pre_kernel<D, DT><<<(unsigned)blocks, 256, 0, stream>>>(
+        static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dO), a.lse, a.dvec, a.lse2, a.dq_accum, a.BH,
+        a.N, a.Npad, accum_elems);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  // 2. dK/dV with dQ partial sums
+  {
+    auto kern = bwd_kv_kernel<D, DT, CAUSAL>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int nb = (a.N + kRows - 1) / kRows;
+    const int ntiles = a.BH * nb;
+    const int grid = ntiles < a.num_sms ? ntiles : a.num_sms;
+    kern<<<grid, kBwdThreads, C::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse2, a.dvec, a.dq_accum,
+                                                        static_cast<uint16_t*>(a.dk), static_cast<uint16_t*>(a.dv),
+                                                        a.BH, a.N, a.Npad, a.scale, a.scale_log2, a.err_word,
+                                                        a.limit_ns);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  // 3. dQ conversion
+  {
+    const size_t n8 = (size_t)a.BH * a.N * D / 8;
+    long long blocks = (long long)((n8 + 255) / 256);
+    if (blocks > 8LL * a.num_sms) blocks = 8LL * a.num_sms;
+    if (blocks < 1) blocks = 1;
+    bwd_dq_kernel<DT><<<(unsigned)blocks, 256, 0, stream>>>(a.dq_accum, static_cast<uint16_t*>(a.dq), a.scale, n8);
+    return cudaGetLastError();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {
+  const int key = (a.d == 128 ? 4 : 0) | (a.dtype == 1 ? 2 : 0) | (a.causal ? 1 : 0);
+  switch (key) {
+    case 0: return launch_bwd_t<64, 0, false>(a, stream);
+    case 1: return launch_bwd_t<64, 0, true>(a, stream);
+    case 2: return launch_bwd_t<64, 1, false>(a, stream);
+    case 3: return launch_bwd_t<64, 1, true>(a, stream);
+    case 4: return launch_bwd_t<128, 0, false>(a, stream);
+    case 5: return launch_bwd_t<128, 0, true>(a, stream);
+    case 6: return launch_bwd_t<128, 1, false>(a, stream);
+    default: return launch_bwd_t<128, 1, true>(a, stream);
+  }
+}
+
+}  // namespace fa

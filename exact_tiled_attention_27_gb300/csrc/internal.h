@@ -1,0 +1,50 @@
+// internal.h -- declarations shared by the host API and the kernel translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Device error word bits: bit 31 = a bounded wait gave up; the low bits name the site.
+constexpr unsigned int kErrTimeoutBit = 0x80000000u;
+
+// Default limit for one mbarrier wait inside a kernel (nanoseconds).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+struct FwdArgs {
+  CUtensorMap tm_q, tm_k, tm_v;  // 3-D maps {d, N, B*H}, box {64, 128, 1}, 128-byte swizzle
+  void* o;
+  float* lse;
+  int BH, N, d, dtype, causal;
+  float scale_log2;              // scale * log2(e)
+  unsigned int* err_word;
+  uint64_t limit_ns;
+  int num_sms;
+};
+
+struct BwdArgs {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;
+  const void* o;
+  const void* dO;
+  const float* lse;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* dvec;        // [B*H*Npad]  D = rowsum(dO o O), 0 on padding rows
+  float* lse2;        // [B*H*Npad]  lse * log2(e), +inf on padding rows
+  float* dq_accum;    // [B*H*N*d]   float32 dQ partial sums
+  int BH, N, Npad, d, dtype, causal;
+  float scale, scale_log2;
+  unsigned int* err_word;
+  uint64_t limit_ns;
+  int num_sms;
+};
+
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_debug_wait(unsigned int* err_word, uint64_t limit_ns, cudaStream_t stream);
+
+}  // namespace fa

@@ -1,0 +1,148 @@
+/*
+ * fa.h -- C ABI of the exact tiled attention library for GB300 (sm_103a).
+ *
+ * The library computes exact scaled-dot-product attention
+ *
+ *     O = softmax(scale * Q K^T) V
+ *
+ * tile by tile with the streaming (online) softmax rescale, so the N x N score
+ * matrix never reaches device memory, and the backward pass that recomputes the
+ * probabilities on chip from Q, K and the saved per-row log-sum-exp.
+ *
+ * Sources (page title and section):
+ *   "Flash Attention" chapter (mlx.void.app), sections "地基：流式 softmax",
+ *     "FlashAttention——把整件事分块塞进 SRAM" and "FlashAttention-2——让每个核心都忙起来";
+ *   review of "FlashAttention: Fast and Memory-Efficient Exact Attention with
+ *     IO-Awareness" (trdm.cn), section "方法细节";
+ *   FlashAttention practitioner article (cf-1.com/news/4497868), sections 1.1, 2.2, 3.1;
+ *   "大模型数学速成（17）：Flash Attention——不物化注意力矩阵", sections 一 to 三.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensors q, k, v, o, dO, dq, dk, dv are DEVICE pointers to contiguous
+ *    (batch, heads, seq, head_dim) arrays -- the layout of the practitioner
+ *    article's section 1.1 -- with element (b, h, n, c) at offset
+ *    ((b*H + h)*N + n)*d + c.  All of them share one 16-bit element type `dtype`.
+ *    Each base address must be 16-byte aligned (the tiles are moved by TMA).
+ *  - lse is a DEVICE pointer to a float32 (batch, heads, seq) array holding the
+ *    natural-log log-sum-exp of each row of scaled scores: lse = m + ln(l), where m
+ *    is the row maximum of scale*q.k and l = sum_j exp(scale*q.k_j - m).  It carries
+ *    the pair (m, l) that the pages' forward keeps for the backward.
+ *  - Causal masking: key j is visible to query i iff j <= i (lower triangle).
+ *  - Supported: d in {64, 128}; N >= 1; B >= 1; H >= 1; B*H*N < 2^31;
+ *    scale finite and > 0; dtype FA_BF16 or FA_FP16.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *    default stream) and runs on the calling thread's current CUDA device.
+ *  - Ownership: the caller owns every buffer.  fa_fwd and fa_bwd allocate no
+ *    device memory; the backward's scratch is the caller's `workspace`.
+ *  - Errors: arguments are validated before any launch; on a validation error
+ *    the call returns the code and writes nothing.  FA_ERR_LAUNCH means a launch
+ *    was rejected by the runtime (cudaGetLastError != success).  Device-side
+ *    pipeline timeouts are reported by fa_get_last_kernel_status.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { FA_BF16 = 0, FA_FP16 = 1 } fa_dtype;
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_NULL = 1,            /* a required pointer is NULL                        */
+  FA_ERR_SHAPE = 2,           /* B, H or N < 1, or B*H*N too large                 */
+  FA_ERR_UNSUPPORTED_D = 3,   /* head_dim not in {64, 128}                         */
+  FA_ERR_DTYPE = 4,           /* dtype not FA_BF16 / FA_FP16                       */
+  FA_ERR_ALIGN = 5,           /* a tensor base address is not 16-byte aligned      */
+  FA_ERR_WORKSPACE = 6,       /* workspace NULL or smaller than fa_bwd_workspace_size */
+  FA_ERR_LAUNCH = 7,          /* the CUDA runtime rejected a launch                */
+  FA_ERR_DEVICE_TIMEOUT = 8,  /* a kernel's bounded pipeline wait gave up          */
+  FA_ERR_NO_DEVICE = 9,       /* no usable sm_100-family device is current         */
+  FA_ERR_SCALE = 10           /* scale not finite or not > 0                       */
+} fa_status;
+
+/*
+ * Forward: O and lse from Q, K, V.
+ *
+ * Computes, for every (b, h), S = scale * Q K^T (masked when `causal` != 0),
+ * O = softmax(S) V and lse = row log-sum-exp of S, tile by tile: each block of
+ * 128 query rows streams the key/value blocks through shared memory, keeps the
+ * running maximum m, running sum l and an unnormalised output in on-chip memory,
+ * rescales them by 2^(m_old - m_new) when the maximum moves, and divides by l once
+ * at the end ("Flash Attention" chapter, sections "地基：流式 softmax" and
+ * "FlashAttention-2"; practitioner article section 2.2).  Blocks wholly above the
+ * causal diagonal are skipped.
+ *
+ *   q, k, v : in,  (B, H, N, d) `dtype`
+ *   o       : out, (B, H, N, d) `dtype`, overwritten
+ *   lse     : out, (B, H, N) float32, overwritten
+ *   Returns FA_OK or an fa_status error code.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int B, int H, int N, int d, float scale, int causal, int dtype, void* stream);
+
+/*
+ * Bytes of device scratch that fa_bwd needs for these sizes: the per-row
+ * D = rowsum(dO o O) and the row log-sum-exp in base 2 (both padded to whole
+ * 128-row blocks), plus a float32 dQ accumulator of B*H*N*d elements.
+ * Returns 0 for invalid sizes.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Backward: dq, dk, dv from Q, K, V, O, dO and lse (as written by fa_fwd).
+ *
+ * Recomputes P = exp(scale*Q K^T - lse) tile by tile on chip instead of reading a
+ * stored probability matrix (review of the FlashAttention paper, "方法细节";
+ * "Flash Attention" chapter, end of the section "FlashAttention——把整件事分块塞进
+ * SRAM").  With D_i = sum_c dO_ic O_ic it forms dV = P^T dO, dP = dO V^T,
+ * dS = P o (dP - D), dQ = scale dS K and dK = scale dS^T Q.  The loop runs over
+ * key/value blocks on the outside and query blocks inside; dQ partial products
+ * are summed in float32 in the workspace and converted at the end, so dq may
+ * differ in the last bits from run to run.
+ *
+ *   q, k, v, o, dO : in,  (B, H, N, d) `dtype`
+ *   lse            : in,  (B, H, N) float32
+ *   dq, dk, dv     : out, (B, H, N, d) `dtype`, overwritten (not accumulated)
+ *   workspace      : scratch, >= fa_bwd_workspace_size(B,H,N,d) bytes, 256-byte
+ *                    aligned; contents on entry are ignored and on exit undefined.
+ *                    Two calls in flight at once must not share it.
+ *   Returns FA_OK or an fa_status error code.
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+           const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+           int B, int H, int N, int d, float scale, int causal, int dtype, void* stream);
+
+/* Static, human-readable text for a status code; never NULL. */
+const char* fa_strerror(int status);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's kernel error
+ * word.  Returns FA_OK, FA_ERR_DEVICE_TIMEOUT when a kernel's bounded mbarrier
+ * wait gave up (the kernel then skipped its remaining work, released its tensor
+ * memory and returned), or FA_ERR_LAUNCH if the stream reported a CUDA error.
+ */
+int fa_get_last_kernel_status(void* stream);
+
+/* Number of streaming multiprocessors the persistent kernels size their grids to
+ * on the current device, or a negative fa_status on error. */
+int fa_device_sm_count(void);
+
+/*
+ * Test hook for the bounded-wait path: launches one block that waits on an
+ * mbarrier nobody arrives on, with a wait limit of `limit_us` microseconds
+ * (clamped to [1, 2000000]).  The kernel gives up, records FA_ERR_DEVICE_TIMEOUT in
+ * the error word and returns; fa_get_last_kernel_status then reports it.  No trap,
+ * no fault.
+ */
+int fa_debug_wait_timeout(unsigned limit_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

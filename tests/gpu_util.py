@@ -1,0 +1,59 @@
+"""Helpers shared by the GPU tests: upload seeded 16-bit bits, read results back as
+float64, the comparison metrics, and the tolerances the parity tests enforce.
+
+Tolerances (stated for the 16-bit inputs against the float64 oracle):
+  O:            max |err| <= 2e-2 and ||err||_2 / ||ref||_2 <= 5e-3
+  lse:          max |err| <= 1e-3
+  dQ, dK, dV:   ||err||_2 / ||ref||_2 <= 1e-2
+"""
+
+import numpy as np
+
+O_MAXABS = 2e-2
+O_RELL2 = 5e-3
+LSE_ABS = 1e-3
+GRAD_RELL2 = 1e-2
+
+
+def torch_dtype(dtype):
+    import torch
+    return torch.bfloat16 if dtype == "bf16" else torch.float16
+
+
+def to_device(bits, dtype):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.view(torch_dtype(dtype)).cuda()
+
+
+def to_f64(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def maxabs(a, b):
+    return float(np.max(np.abs(a - b))) if a.size else 0.0
+
+
+def rel_l2(a, ref):
+    den = float(np.linalg.norm(ref))
+    num = float(np.linalg.norm(a - ref))
+    return num / den if den > 0 else num
+
+
+def check_forward(o, lse, o_ref, lse_ref, label=""):
+    ma, rl, la = maxabs(o, o_ref), rel_l2(o, o_ref), maxabs(lse, lse_ref)
+    msg = f"{label} O maxabs={ma:.3e} relL2={rl:.3e} lse abs={la:.3e}"
+    print(msg)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse)), msg
+    assert ma <= O_MAXABS and rl <= O_RELL2 and la <= LSE_ABS, msg
+    return ma, rl, la
+
+
+def check_backward(grads, refs, label=""):
+    errs = [rel_l2(g, r) for g, r in zip(grads, refs)]
+    msg = f"{label} relL2 dQ={errs[0]:.3e} dK={errs[1]:.3e} dV={errs[2]:.3e}"
+    print(msg)
+    for g in grads:
+        assert np.all(np.isfinite(g)), msg
+    assert max(errs) <= GRAD_RELL2, msg
+    return errs

@@ -1,0 +1,131 @@
+"""Boundary tests that need no GPU: the library builds, loads, exports every entry
+point include/fa.h declares, and rejects invalid arguments before touching a device."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_tiled_attention_27_gb300 import binding, build
+from exact_tiled_attention_27_gb300.inputs import WORKLOADS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?\w+\s*\**\s+(fa_\w+)\s*\(", text, flags=re.M)
+
+
+def test_header_declares_expected_entry_points():
+    names = set(declared_functions())
+    assert {"fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_strerror", "fa_get_last_kernel_status"} <= names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in fa.h but not exported"
+
+
+def test_status_enum_matches_binding():
+    text = open(HEADER).read()
+    for name, code in re.findall(r"(FA_(?:OK|ERR_\w+))\s*=\s*(\d+)", text):
+        assert binding.STATUS[int(code)] == name
+
+
+def test_strerror_covers_every_code(lib):
+    for code in binding.STATUS:
+        s = lib.fa_strerror(code).decode()
+        assert s and s != "unknown status"
+    assert lib.fa_strerror(12345).decode() == "unknown status"
+
+
+P = ctypes.c_void_p(0x10000)      # a 16-byte aligned stand-in; never dereferenced on error paths
+PM = ctypes.c_void_p(0x10008)     # misaligned
+NULL = ctypes.c_void_p(0)
+
+
+def fwd(lib, q=P, k=P, v=P, o=P, lse=P, B=1, H=1, N=128, d=64, scale=0.125, causal=0, dtype=0):
+    return lib.fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, NULL)
+
+
+def bwd(lib, ws=P, ws_bytes=None, q=P, B=1, H=1, N=128, d=64, scale=0.125, dtype=0, dq=P):
+    if ws_bytes is None:
+        ws_bytes = lib.fa_bwd_workspace_size(B, H, N, d) if B > 0 and H > 0 and N > 0 else 0
+    return lib.fa_bwd(q, P, P, P, P, P, dq, P, P, ws, ws_bytes, B, H, N, d, scale, 0, dtype, NULL)
+
+
+def test_forward_validation_codes(lib):
+    C = binding.STATUS_CODE
+    assert fwd(lib, dtype=2) == C["FA_ERR_DTYPE"]
+    assert fwd(lib, d=32) == C["FA_ERR_UNSUPPORTED_D"]
+    assert fwd(lib, d=96) == C["FA_ERR_UNSUPPORTED_D"]
+    assert fwd(lib, B=0) == C["FA_ERR_SHAPE"]
+    assert fwd(lib, H=-1) == C["FA_ERR_SHAPE"]
+    assert fwd(lib, N=0) == C["FA_ERR_SHAPE"]
+    assert fwd(lib, B=1 << 16, H=1 << 16) == C["FA_ERR_SHAPE"]
+    assert fwd(lib, scale=0.0) == C["FA_ERR_SCALE"]
+    assert fwd(lib, scale=-1.0) == C["FA_ERR_SCALE"]
+    assert fwd(lib, scale=float("nan")) == C["FA_ERR_SCALE"]
+    assert fwd(lib, scale=float("inf")) == C["FA_ERR_SCALE"]
+    assert fwd(lib, q=NULL) == C["FA_ERR_NULL"]
+    assert fwd(lib, lse=NULL) == C["FA_ERR_NULL"]
+    assert fwd(lib, k=PM) == C["FA_ERR_ALIGN"]
+    assert fwd(lib, o=PM) == C["FA_ERR_ALIGN"]
+
+
+def test_backward_validation_codes(lib):
+    C = binding.STATUS_CODE
+    assert bwd(lib, dtype=7) == C["FA_ERR_DTYPE"]
+    assert bwd(lib, d=256) == C["FA_ERR_UNSUPPORTED_D"]
+    assert bwd(lib, N=0) == C["FA_ERR_SHAPE"]
+    assert bwd(lib, scale=float("nan")) == C["FA_ERR_SCALE"]
+    assert bwd(lib, q=NULL) == C["FA_ERR_NULL"]
+    assert bwd(lib, dq=PM) == C["FA_ERR_ALIGN"]
+    assert bwd(lib, ws=NULL) == C["FA_ERR_WORKSPACE"]
+    need = lib.fa_bwd_workspace_size(1, 1, 128, 64)
+    assert bwd(lib, ws_bytes=need - 1) == C["FA_ERR_WORKSPACE"]
+    assert bwd(lib, ws=ctypes.c_void_p(0x10010)) == C["FA_ERR_WORKSPACE"]   # not 256-byte aligned
+
+
+def test_valid_arguments_without_gpu_report_no_device(lib):
+    """On a machine with no CUDA device the call gets past validation and stops at
+    the device check, with nothing launched."""
+    try:
+        import torch
+        if torch.cuda.is_available():
+            pytest.skip("a GPU is present")
+    except ImportError:
+        pass
+    assert fwd(lib) == binding.STATUS_CODE["FA_ERR_NO_DEVICE"]
+    assert bwd(lib) == binding.STATUS_CODE["FA_ERR_NO_DEVICE"]
+    assert lib.fa_get_last_kernel_status(NULL) == binding.STATUS_CODE["FA_ERR_NO_DEVICE"]
+
+
+@pytest.mark.parametrize("B,H,N,d", [(1, 1, 1, 64), (2, 3, 129, 128), (8, 12, 1024, 64), (4, 16, 8192, 64)])
+def test_workspace_size_formula(lib, B, H, N, d):
+    npad = (N + 127) // 128 * 128
+
+    def up(x):
+        return (x + 255) // 256 * 256
+
+    expect = 2 * up(B * H * npad * 4) + up(B * H * N * d * 4)
+    assert lib.fa_bwd_workspace_size(B, H, N, d) == expect
+    assert lib.fa_bwd_workspace_size(0, H, N, d) == 0
+    assert lib.fa_bwd_workspace_size(B, H, N, 80) == 0
+
+
+def test_workloads_table_matches_the_stated_shapes():
+    assert WORKLOADS["c2_gpt2s"]["B"] * WORKLOADS["c2_gpt2s"]["H"] == 96
+    for name, w in WORKLOADS.items():
+        if name.startswith("c5_"):
+            assert w["B"] * w["N"] == 65536 and w["mult"] == 3.0
