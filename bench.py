@@ -1,0 +1,421 @@
+#!/usr/bin/env python
+"""Attention throughput on GB300: TFLOPS of the forward and of forward+backward.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--e2e-steps E] [--cpu-seconds S]
+
+A step is one forward (fa_fwd) and one backward (the three launches of fa_bwd) over
+one batch of seeded synthetic inputs already resident in device memory.  Between
+timed steps a 256 MiB buffer is written to flush the 129 MB L2; the flush is outside
+the CUDA-event brackets.  FLOPs follow the usual convention: forward 4*B*H*N^2*d,
+backward 10*B*H*N^2*d, both halved under the causal mask.
+
+Prints one JSON line (rank 0).  With --impl reference the float64 CPU oracle is timed
+instead, on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from exact_tiled_attention_27_gb300.inputs import WORKLOADS, workload_case  # noqa: E402
+
+METRIC = "attention TFLOPS fwd and fwd+bwd (bf16, causal/non) and % of GB300 BF16 tensor peak"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "c2_gpt2s"
+FALLBACK_PEAK_TFLOPS = 1900.0
+FALLBACK_SUSTAINED_TFLOPS = 1700.0
+
+
+def flops(w, which):
+    B, H, N, d = w["B"], w["H"], w["N"], w["d"]
+    base = B * H * N * N * d
+    f = {"fwd": 4 * base, "bwd": 10 * base, "fwd_bwd": 14 * base}[which]
+    return f / 2 if w["causal"] else f
+
+
+def describe(name, w):
+    parts = f"B={w['B']} H={w['H']} N={w['N']} d={w['d']} {w['dtype']} {'causal' if w['causal'] else 'non-causal'}"
+    mult = f" inputs x{w['mult']:g}" if w["mult"] != 1.0 else ""
+    return f"{name}: {parts}{mult} {'fwd+bwd' if w['backward'] else 'fwd'}"
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["bf16_tflops"]), float(j.get("bf16_tflops_sustained", j["bf16_tflops"])), "measured"
+    return FALLBACK_PEAK_TFLOPS, FALLBACK_SUSTAINED_TFLOPS, "fallback"
+
+
+# ---------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.t is not None:
+            self.t.join(timeout=5)
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- our arm
+def run_ours(args, w, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    from exact_tiled_attention_27_gb300 import build as fa_build
+    from exact_tiled_attention_27_gb300 import binding as fa
+
+    fa_build.build()
+    lib = fa.load_library()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+    sh = fa._stream_handle(stream)
+    case = workload_case(args.workload)
+    tdt = torch.bfloat16 if w["dtype"] == "bf16" else torch.float16
+    dcode = fa.FA_BF16 if w["dtype"] == "bf16" else fa.FA_FP16
+    B, H, N, d = w["B"], w["H"], w["N"], w["d"]
+    causal = 1 if w["causal"] else 0
+    scale = case.scale
+
+    def host(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(tdt).pin_memory()
+
+    h_in = [host(case.q), host(case.k), host(case.v)] + ([host(case.do)] if w["backward"] else [])
+    d_in = [t.to(dev) for t in h_in]
+    q, k, v = d_in[:3]
+    do = d_in[3] if w["backward"] else None
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3)) if w["backward"] else (None, None, None)
+    ws_bytes = fa.workspace_size(B, H, N, d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    P = fa._ptr
+
+    def call(st, what):
+        if st != 0:
+            raise fa.FaError(st, what)
+
+    def fwd():
+        call(lib.fa_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, scale, causal, dcode, sh), "fa_fwd")
+
+    bwd_args = None
+    if w["backward"]:
+        bwd_args = lambda: (P(q), P(k), P(v), P(o), P(do), P(lse), P(dq), P(dk), P(dv), P(ws), ws_bytes,  # noqa: E731
+                            B, H, N, d, scale, causal, dcode, sh)
+
+    stages = []
+    if w["backward"]:
+        stages = [lib.fa_bwd_preprocess, lib.fa_bwd_dkdv, lib.fa_bwd_dq_convert]
+
+    n_ev = 2 + len(stages)
+    launches_per_step = 1 + len(stages)
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        fwd()
+        if evs:
+            evs[1].record(stream)
+        for i, fn in enumerate(stages):
+            call(fn(*bwd_args()), fn.__name__)
+            if evs:
+                evs[2 + i].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if fa.last_kernel_status() != 0:
+        raise RuntimeError("a kernel reported a pipeline timeout during warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.2)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        step(ev[i])
+    torch.cuda.synchronize()
+    wall1 = time.perf_counter()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+    status = fa.last_kernel_status()
+    if status != 0:
+        raise RuntimeError(f"a kernel reported {fa.STATUS.get(status)} in the timed region")
+
+    seg = [[ev[i][j].elapsed_time(ev[i][j + 1]) for j in range(n_ev - 1)] for i in range(args.steps)]
+    t_fwd = statistics.mean(s[0] for s in seg)
+    t_stage = [statistics.mean(s[1 + j] for s in seg) for j in range(len(stages))]
+    t_bwd = sum(t_stage)
+    t_step = t_fwd + t_bwd
+    if world > 1:
+        t = torch.tensor([t_step, t_fwd, t_bwd], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_step, t_fwd, t_bwd = (float(x) for x in t.tolist())
+
+    f_fwd = flops(w, "fwd")
+    f_bwd = flops(w, "bwd") if w["backward"] else 0.0
+    f_step = f_fwd + f_bwd
+    value = world * f_step / (t_step * 1e-3) / 1e12
+    peak_burst, peak_sus, peak_src = measured_peaks()
+
+    # ---------------------------------------------------------------- end to end (host buffers)
+    e2e = None
+    if args.e2e_steps > 0:
+        h_out = [torch.empty_like(o, device="cpu").pin_memory(), torch.empty_like(lse, device="cpu").pin_memory()]
+        if w["backward"]:
+            h_out += [torch.empty_like(q, device="cpu").pin_memory() for _ in range(3)]
+        d_out = [o, lse] + ([dq, dk, dv] if w["backward"] else [])
+        h2d = sum(t.numel() * t.element_size() for t in h_in)
+        d2h = sum(t.numel() * t.element_size() for t in h_out)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for it in range(args.e2e_steps + 2):
+            if it == 2:
+                e0.record(stream)
+            for hsrc, ddst in zip(h_in, d_in):
+                ddst.copy_(hsrc, non_blocking=True)
+            fwd()
+            for fn in stages:
+                call(fn(*bwd_args()), fn.__name__)
+            for dsrc, hdst in zip(d_out, h_out):
+                hdst.copy_(dsrc, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t_e2e = e0.elapsed_time(e1) / args.e2e_steps
+        e2e = {"value": round(world * f_step / (t_e2e * 1e-3) / 1e12, 3), "unit": UNIT,
+               "ms_per_step": round(t_e2e, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    # dominant kernel: the dK/dV kernel when there is a backward, else the forward
+    if w["backward"]:
+        dom_name, dom_t, dom_f = "bwd_kv_kernel", t_stage[1], f_bwd
+    else:
+        dom_name, dom_t, dom_f = "fwd_kernel", t_fwd, f_fwd
+    achieved = dom_f / (dom_t * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "kernel": dom_name, "achieved": round(achieved, 2), "peak": peak_sus,
+                "unit": UNIT, "frac": round(achieved / peak_sus, 4),
+                "peak_source": f"{peak_src} bf16 cuBLAS sustained (kernel timed inside a seconds-long loop)",
+                "frac_of_burst_peak": round(achieved / peak_burst, 4),
+                "traffic": traffic_for(dom_name, args.workload)}
+    result = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w["dtype"], "data": "synthetic (seeded i.i.d. N(0,1) 16-bit inputs)",
+        "config": {"workload": describe(args.workload, w), "B": B, "H": H, "N": N, "d": d, "causal": bool(causal),
+                   "l2": "flushed between steps by a 256 MiB write outside the timed brackets",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "tflops": {"fwd": round(f_fwd / (t_fwd * 1e-3) / 1e12, 2),
+                   "bwd": round(f_bwd / (t_bwd * 1e-3) / 1e12, 2) if w["backward"] else None,
+                   "fwd_bwd": round(f_step / (t_step * 1e-3) / 1e12, 2)},
+        "pct_of_peak": {"fwd": round(100 * f_fwd / (t_fwd * 1e-3) / 1e12 / peak_burst, 2),
+                        "bwd": round(100 * f_bwd / (t_bwd * 1e-3) / 1e12 / peak_burst, 2) if w["backward"] else None,
+                        "fwd_bwd": round(100 * f_step / (t_step * 1e-3) / 1e12 / peak_burst, 2),
+                        "peak": f"{peak_burst} TFLOP/s dense bf16 ({peak_src}, burst)"},
+        "ms": {"fwd": round(t_fwd, 5), "bwd": round(t_bwd, 5),
+               "bwd_stages": [round(x, 5) for x in t_stage]},
+        "roofline": roofline,
+        "gpu_launches": launches_per_step * args.steps,
+        "wall_s_timed": round(wall1 - wall0, 3),
+    }
+    if clk:
+        result["clocks"] = clk
+    if e2e:
+        result["e2e"] = e2e
+    return result
+
+
+def traffic_for(kernel, workload):
+    """DRAM bytes per launch from a committed ncu capture of the current kernel, if any."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        entry = j.get(f"{kernel}:{workload}")
+        return entry.get("bytes_per_launch") if entry else None
+    except (OSError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------- oracle arm
+def oracle_sample(w, seconds, max_heads=None):
+    """Time the float64 oracle on whole (b, h) heads of the workload until `seconds`."""
+    import numpy as np
+
+    import oracle
+    case = workload_case_cached(w)
+    q64, k64, v64 = case.f64("q"), case.f64("k"), case.f64("v")
+    do64 = case.f64("do") if w["backward"] else None
+    heads = [(b, h) for b in range(w["B"]) for h in range(w["H"])]
+    rb = 1024 if w["N"] > 8192 else None
+    done = 0
+    t0 = time.perf_counter()
+    for b, h in heads:
+        oracle.attn_head_fwd(q64[b, h], k64[b, h], v64[b, h], case.scale, w["causal"], rb)
+        if w["backward"]:
+            oracle.attn_head_bwd(q64[b, h], k64[b, h], v64[b, h], do64[b, h], case.scale, w["causal"], rb)
+        done += 1
+        if time.perf_counter() - t0 >= seconds or (max_heads and done >= max_heads):
+            break
+    el = time.perf_counter() - t0
+    per_head = (flops(w, "fwd_bwd") if w["backward"] else flops(w, "fwd")) / (w["B"] * w["H"])
+    del np
+    return done, el, per_head * done / el / 1e12
+
+
+_CASE_CACHE = {}
+
+
+def workload_case_cached(w):
+    key = id(w)
+    if key not in _CASE_CACHE:
+        name = [n for n, x in WORKLOADS.items() if x is w][0]
+        _CASE_CACHE[key] = workload_case(name)
+    return _CASE_CACHE[key]
+
+
+def run_reference(args, w):
+    # warm-up and timed steps, each one bounded sample of whole heads
+    for _ in range(args.warmup):
+        oracle_sample(w, 0.0, max_heads=1)
+    vals, heads_total, el_total = [], 0, 0.0
+    for _ in range(args.steps):
+        nh, el, tf = oracle_sample(w, args.cpu_seconds / max(args.steps, 1), max_heads=None)
+        vals.append(tf)
+        heads_total += nh
+        el_total += el
+    value = statistics.mean(vals)
+    cores = os.cpu_count()
+    sample = (f"{heads_total} whole (b,h) heads of {w['B'] * w['H']} over {args.steps} steps, "
+              f"{'forward+backward' if w['backward'] else 'forward'}, float64 numpy, {el_total:.1f} s")
+    return {"metric": METRIC, "value": round(value, 6), "unit": UNIT, "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * el_total / max(args.steps, 1), 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded i.i.d. N(0,1) 16-bit inputs widened to float64)",
+            "config": {"workload": describe(args.workload, w)},
+            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="wall-clock budget of the oracle's CPU-baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = WORKLOADS[args.workload]
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        steps = max(1, min(args.steps, 20))
+        args.steps = steps
+        print(json.dumps(run_reference(args, w)))
+        return 0
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    result = run_ours(args, w, rank, world, local_rank)
+    if rank == 0 and not args.no_cpu_baseline:
+        nh, el, tf = oracle_sample(w, args.cpu_seconds)
+        result["cpu_baseline"] = {
+            "value": round(tf, 6), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": (f"{nh} whole (b,h) heads of {w['B'] * w['H']}, "
+                       f"{'forward+backward' if w['backward'] else 'forward'}, float64 numpy, {el:.1f} s")}
+    if rank == 0:
+        print(json.dumps(result))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

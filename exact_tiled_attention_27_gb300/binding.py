@@ -53,6 +53,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.fa_bwd_workspace_size.restype = sz
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, f, i, i, vp]
         lib.fa_bwd.restype = i
+        for name in ("fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq_convert"):
+            fn = getattr(lib, name)
+            fn.argtypes = lib.fa_bwd.argtypes
+            fn.restype = i
         lib.fa_strerror.argtypes = [i]
         lib.fa_strerror.restype = ctypes.c_char_p
         lib.fa_get_last_kernel_status.argtypes = [vp]
@@ -140,11 +144,13 @@ def forward(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None):
 
 
 def backward(q, k, v, o, do, lse, scale=None, causal=False, dq=None, dk=None, dv=None, workspace=None,
-             stream=None):
+             stream=None, stage=None):
     """Exact attention backward.  Returns (dq, dk, dv) like q.
 
     ``workspace`` (optional) is a CUDA uint8 tensor of at least workspace_size(B,H,N,d)
-    bytes; one is allocated through torch when it is not given.
+    bytes; one is allocated through torch when it is not given.  ``stage`` runs one of
+    the three launches of the backward ("preprocess", "dkdv", "dq_convert"); calling the
+    three in order with the same workspace equals the default (all three).
     """
     torch = _torch()
     B, H, N, d = q.shape
@@ -159,15 +165,17 @@ def backward(q, k, v, o, do, lse, scale=None, causal=False, dq=None, dk=None, dv
     for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
         _check_bhnd(name, t, (B, H, N, d), q.dtype)
     need = workspace_size(B, H, N, d)
+    fn_name = {None: "fa_bwd", "preprocess": "fa_bwd_preprocess", "dkdv": "fa_bwd_dkdv",
+               "dq_convert": "fa_bwd_dq_convert"}[stage]
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     if workspace.numel() * workspace.element_size() < need:
         raise ValueError(f"workspace too small: need {need} bytes")
-    st = load_library().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
-                               _ptr(dv), _ptr(workspace), need, B, H, N, d, scale, 1 if causal else 0,
-                               _dtype_code(q), _stream_handle(stream))
+    fn = getattr(load_library(), fn_name)
+    st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+            _ptr(workspace), need, B, H, N, d, scale, 1 if causal else 0, _dtype_code(q), _stream_handle(stream))
     if st != 0:
-        raise FaError(st, "fa_bwd")
+        raise FaError(st, fn_name)
     return dq, dk, dv
 
 

@@ -178,9 +178,9 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   return ws_layout(B, H, N, d).total;
 }
 
-int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse, void* dq,
-           void* dk, void* dv, void* workspace, size_t ws_bytes, int B, int H, int N, int d, float scale, int causal,
-           int dtype, void* stream) {
+static int bwd_common(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                      void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes, int B, int H, int N, int d,
+                      float scale, int causal, int dtype, void* stream, int stages) {
   int st = check_common(B, H, N, d, scale, dtype);
   if (st != FA_OK) return st;
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_NULL;
@@ -219,7 +219,35 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   a.err_word = dev->err_word;
   a.limit_ns = kWaitLimitNs;
   a.num_sms = dev->num_sms;
-  return launch_bwd(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+  return launch_bwd(a, static_cast<cudaStream_t>(stream), stages) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse, void* dq,
+           void* dk, void* dv, void* workspace, size_t ws_bytes, int B, int H, int N, int d, float scale, int causal,
+           int dtype, void* stream) {
+  return bwd_common(q, k, v, o, dO, lse, dq, dk, dv, workspace, ws_bytes, B, H, N, d, scale, causal, dtype, stream,
+                    kBwdStagePre | kBwdStageKV | kBwdStageDQ);
+}
+
+int fa_bwd_preprocess(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                      void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes, int B, int H, int N, int d,
+                      float scale, int causal, int dtype, void* stream) {
+  return bwd_common(q, k, v, o, dO, lse, dq, dk, dv, workspace, ws_bytes, B, H, N, d, scale, causal, dtype, stream,
+                    kBwdStagePre);
+}
+
+int fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes, int B, int H, int N, int d,
+                float scale, int causal, int dtype, void* stream) {
+  return bwd_common(q, k, v, o, dO, lse, dq, dk, dv, workspace, ws_bytes, B, H, N, d, scale, causal, dtype, stream,
+                    kBwdStageKV);
+}
+
+int fa_bwd_dq_convert(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                      void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes, int B, int H, int N, int d,
+                      float scale, int causal, int dtype, void* stream) {
+  return bwd_common(q, k, v, o, dO, lse, dq, dk, dv, workspace, ws_bytes, B, H, N, d, scale, causal, dtype, stream,
+                    kBwdStageDQ);
 }
 
 const char* fa_strerror(int status) {

@@ -485,10 +485,9 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ a
 }
 
 template <int D, int DT, bool CAUSAL>
-cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
+cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int stages) {
   using C = BwdCfg<D>;
-  // 1. preprocess
-  {
+  if (stages & kBwdStagePre) {
     constexpr int kTPR = D / 8;
     const long long threads = (long long)a.BH * a.Npad * kTPR;
     long long blocks = (threads + 255) / 256;
@@ -501,8 +500,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  // 2. dK/dV with dQ partial sums
-  {
+  if (stages & kBwdStageKV) {
     auto kern = bwd_kv_kernel<D, DT, CAUSAL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -516,8 +514,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  // 3. dQ conversion
-  {
+  if (stages & kBwdStageDQ) {
     const size_t n8 = (size_t)a.BH * a.N * D / 8;
     long long blocks = (long long)((n8 + 255) / 256);
     if (blocks > 8LL * a.num_sms) blocks = 8LL * a.num_sms;
@@ -525,21 +522,22 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
     bwd_dq_kernel<DT><<<(unsigned)blocks, 256, 0, stream>>>(a.dq_accum, static_cast<uint16_t*>(a.dq), a.scale, n8);
     return cudaGetLastError();
   }
+  return cudaSuccess;
 }
 
 }  // namespace
 
-cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream, int stages) {
   const int key = (a.d == 128 ? 4 : 0) | (a.dtype == 1 ? 2 : 0) | (a.causal ? 1 : 0);
   switch (key) {
-    case 0: return launch_bwd_t<64, 0, false>(a, stream);
-    case 1: return launch_bwd_t<64, 0, true>(a, stream);
-    case 2: return launch_bwd_t<64, 1, false>(a, stream);
-    case 3: return launch_bwd_t<64, 1, true>(a, stream);
-    case 4: return launch_bwd_t<128, 0, false>(a, stream);
-    case 5: return launch_bwd_t<128, 0, true>(a, stream);
-    case 6: return launch_bwd_t<128, 1, false>(a, stream);
-    default: return launch_bwd_t<128, 1, true>(a, stream);
+    case 0: return launch_bwd_t<64, 0, false>(a, stream, stages);
+    case 1: return launch_bwd_t<64, 0, true>(a, stream, stages);
+    case 2: return launch_bwd_t<64, 1, false>(a, stream, stages);
+    case 3: return launch_bwd_t<64, 1, true>(a, stream, stages);
+    case 4: return launch_bwd_t<128, 0, false>(a, stream, stages);
+    case 5: return launch_bwd_t<128, 0, true>(a, stream, stages);
+    case 6: return launch_bwd_t<128, 1, false>(a, stream, stages);
+    default: return launch_bwd_t<128, 1, true>(a, stream, stages);
   }
 }
 

@@ -44,7 +44,12 @@ struct BwdArgs {
 };
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
-cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
+// Backward stages: preprocess (D, lse2, zeroed accumulator), the dK/dV kernel with
+// dQ partial sums, and the dQ conversion.
+constexpr int kBwdStagePre = 1;
+constexpr int kBwdStageKV = 2;
+constexpr int kBwdStageDQ = 4;
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream, int stages);
 cudaError_t launch_debug_wait(unsigned int* err_word, uint64_t limit_ns, cudaStream_t stream);
 
 }  // namespace fa

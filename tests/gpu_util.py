@@ -2,7 +2,12 @@
 float64, the comparison metrics, and the tolerances the parity tests enforce.
 
 Tolerances (stated for the 16-bit inputs against the float64 oracle):
-  O:            max |err| <= 2e-2 and ||err||_2 / ||ref||_2 <= 5e-3
+  O:            max |err| <= 2e-2 * mult and ||err||_2 / ||ref||_2 <= 5e-3, where mult
+                is the factor the Gaussian inputs were multiplied by (1 for unit-scale
+                data, 3 for the "x3" sweep).  O is a convex combination of V rows, so its
+                magnitude -- and the spacing of the 16-bit grid it is rounded to --
+                grows with mult; at mult = 3 the exact O rounded to bf16 already errs by
+                up to 0.031 > 2e-2.
   lse:          max |err| <= 1e-3
   dQ, dK, dV:   ||err||_2 / ||ref||_2 <= 1e-2
 """
@@ -40,12 +45,12 @@ def rel_l2(a, ref):
     return num / den if den > 0 else num
 
 
-def check_forward(o, lse, o_ref, lse_ref, label=""):
+def check_forward(o, lse, o_ref, lse_ref, label="", mult=1.0):
     ma, rl, la = maxabs(o, o_ref), rel_l2(o, o_ref), maxabs(lse, lse_ref)
-    msg = f"{label} O maxabs={ma:.3e} relL2={rl:.3e} lse abs={la:.3e}"
+    msg = f"{label} O maxabs={ma:.3e} (bound {O_MAXABS * mult:.1e}) relL2={rl:.3e} lse abs={la:.3e}"
     print(msg)
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse)), msg
-    assert ma <= O_MAXABS and rl <= O_RELL2 and la <= LSE_ABS, msg
+    assert ma <= O_MAXABS * mult and rl <= O_RELL2 and la <= LSE_ABS, msg
     return ma, rl, la
 
 
