@@ -20,7 +20,7 @@ FA_BF16, FA_FP16 = 0, 1
 STATUS = {
     0: "FA_OK", 1: "FA_ERR_NULL", 2: "FA_ERR_SHAPE", 3: "FA_ERR_UNSUPPORTED_D", 4: "FA_ERR_DTYPE",
     5: "FA_ERR_ALIGN", 6: "FA_ERR_WORKSPACE", 7: "FA_ERR_LAUNCH", 8: "FA_ERR_DEVICE_TIMEOUT",
-    9: "FA_ERR_NO_DEVICE", 10: "FA_ERR_SCALE",
+    9: "FA_ERR_NO_DEVICE", 10: "FA_ERR_SCALE", 11: "FA_ERR_SCRATCH_LIMIT",
 }
 STATUS_CODE = {v: k for k, v in STATUS.items()}
 
@@ -57,6 +57,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             fn = getattr(lib, name)
             fn.argtypes = lib.fa_bwd.argtypes
             fn.restype = i
+        lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
+        lib.fa_bwd_noalloc.restype = i
+        lib.fa_bwd_noalloc_max_scratch.argtypes = []
+        lib.fa_bwd_noalloc_max_scratch.restype = sz
         lib.fa_strerror.argtypes = [i]
         lib.fa_strerror.restype = ctypes.c_char_p
         lib.fa_get_last_kernel_status.argtypes = [vp]

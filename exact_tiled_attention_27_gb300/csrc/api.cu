@@ -263,6 +263,8 @@ const char* fa_strerror(int status) {
     case FA_ERR_DEVICE_TIMEOUT: return "a kernel's bounded pipeline wait gave up";
     case FA_ERR_NO_DEVICE: return "no usable sm_100-family CUDA device is current";
     case FA_ERR_SCALE: return "scale must be finite and > 0";
+    case FA_ERR_SCRATCH_LIMIT:
+      return "fa_bwd_noalloc: these sizes need more scratch than its built-in array (fa_bwd_noalloc_max_scratch)";
     default: return "unknown status";
   }
 }

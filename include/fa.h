@@ -62,7 +62,9 @@ typedef enum {
   FA_ERR_LAUNCH = 7,          /* the CUDA runtime rejected a launch                */
   FA_ERR_DEVICE_TIMEOUT = 8,  /* a kernel's bounded pipeline wait gave up          */
   FA_ERR_NO_DEVICE = 9,       /* no usable sm_100-family device is current         */
-  FA_ERR_SCALE = 10           /* scale not finite or not > 0                       */
+  FA_ERR_SCALE = 10,          /* scale not finite or not > 0                       */
+  FA_ERR_SCRATCH_LIMIT = 11   /* fa_bwd_noalloc: the problem needs more scratch than
+                                 the library's built-in array holds                 */
 } fa_status;
 
 /*
@@ -137,6 +139,36 @@ int fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* o, cons
 int fa_bwd_dq_convert(const void* q, const void* k, const void* v, const void* o, const void* dO,
                       const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
                       int B, int H, int N, int d, float scale, int causal, int dtype, void* stream);
+
+/*
+ * Backward without any device allocation (no counterpart in the paper: this entry
+ * point exists for callers, not for the method).
+ *
+ * Same computation, arguments and validation as fa_bwd, minus the workspace.  It is
+ * for callers that cannot allocate device memory when they run the backward -- for
+ * example, code running under a framework whose caching allocator already holds the
+ * device's memory, a plugin host that passes a kernel library nothing but the tensors
+ * it works on, or a latency-critical path that cannot afford cudaMalloc's possible
+ * device synchronisation or failure.  Its scratch is a fixed array of
+ * fa_bwd_noalloc_max_scratch() bytes (32 MiB) that the library keeps in device memory
+ * on every GPU where it is loaded, until the process exits.
+ *
+ *   - Sizes whose fa_bwd_workspace_size exceeds that limit are rejected with
+ *     FA_ERR_SCRATCH_LIMIT before anything is launched (at d = 64 the limit is
+ *     about 8.1 million elements of B*H*N*d).
+ *   - No cudaMalloc, cudaFree or other allocating call is made.
+ *   - The first call on each device looks up the array's device address (with that
+ *     device current); make that first call before any stream capture.
+ *   - Every call on a device shares the one array and it keeps the last call's
+ *     contents (each call re-zeroes what must start at zero).  Calls whose work
+ *     overlaps on the GPU -- two streams, or two host threads -- race on it.
+ */
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                   const float* lse, void* dq, void* dk, void* dv,
+                   int B, int H, int N, int d, float scale, int causal, int dtype, void* stream);
+
+/* Size in bytes of fa_bwd_noalloc's built-in scratch array. */
+size_t fa_bwd_noalloc_max_scratch(void);
 
 /* Static, human-readable text for a status code; never NULL. */
 const char* fa_strerror(int status);

@@ -129,3 +129,27 @@ def test_workloads_table_matches_the_stated_shapes():
     for name, w in WORKLOADS.items():
         if name.startswith("c5_"):
             assert w["B"] * w["N"] == 65536 and w["mult"] == 3.0
+
+
+def test_noalloc_validates_like_fa_bwd_and_checks_its_limit(lib):
+    """fa_bwd_noalloc reports fa_bwd's validation errors, refuses sizes beyond its
+    built-in scratch array, and without a GPU stops at the device check."""
+    C = binding.STATUS_CODE
+
+    def call(B=1, H=1, N=128, d=64, dtype=0, q=P, scale=0.125):
+        return lib.fa_bwd_noalloc(q, P, P, P, P, P, P, P, P, B, H, N, d, scale, 0, dtype, NULL)
+
+    assert call(dtype=3) == C["FA_ERR_DTYPE"]
+    assert call(d=48) == C["FA_ERR_UNSUPPORTED_D"]
+    assert call(q=NULL) == C["FA_ERR_NULL"]
+    assert call(q=PM) == C["FA_ERR_ALIGN"]
+    assert call(scale=-2.0) == C["FA_ERR_SCALE"]
+    assert call(B=2, H=16, N=4096) == C["FA_ERR_SCRATCH_LIMIT"]
+    assert lib.fa_bwd_workspace_size(2, 16, 4096, 64) > lib.fa_bwd_noalloc_max_scratch() == 32 << 20
+    try:
+        import torch
+        has_gpu = torch.cuda.is_available()
+    except ImportError:
+        has_gpu = False
+    if not has_gpu:
+        assert call() == C["FA_ERR_NO_DEVICE"]
