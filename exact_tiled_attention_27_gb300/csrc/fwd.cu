@@ -280,24 +280,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 128; ++c)
             if (kbase + c > lim) s[c] = -INFINITY;
         }
-        float mx = s[0];
+        // row maximum: 8 independent chains, then a tree
+        float m8[8];
 #pragma unroll
-        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+        for (int i = 0; i < 8; ++i) m8[i] = s[i];
+#pragma unroll
+        for (int c = 8; c < 128; c += 8)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], s[c + i]);
+        const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
         const float mc = mx * scale_log2;
         const float m_new = (mc > m + kRescaleThreshold) ? mc : m;
         const float alpha = ex2_approx(m - m_new);
         const float neg_m = -m_new;
-        float sum0 = 0.f, sum1 = 0.f;
+        float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         uint32_t pk[64];
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
           const float p0 = ex2_approx(fmaf(s[2 * c], scale_log2, neg_m));
           const float p1 = ex2_approx(fmaf(s[2 * c + 1], scale_log2, neg_m));
-          sum0 += p0;
-          sum1 += p1;
+          l8[(2 * c) & 7] += p0;
+          l8[(2 * c + 1) & 7] += p1;
           pk[c] = pack2<DT>(p0, p1);
         }
-        l = l * alpha + (sum0 + sum1);
+        const float rowsum = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+        l = l * alpha + rowsum;
         tmem_st32(tmem + lane_base + C::kTmP + sb * 64, pk);
         tmem_st32(tmem + lane_base + C::kTmP + sb * 64 + 32, pk + 32);
         if (j > 0) {
