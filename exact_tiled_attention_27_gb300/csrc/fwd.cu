@@ -1,29 +1,43 @@
 // fwd.cu -- forward kernel of exact tiled attention for sm_103a.
 //
-// One persistent CTA per SM walks (batch*head, 128-row query block) tiles, heaviest
-// causal tiles first.  Inside a CTA the work is split by role:
+// One persistent CTA per SM walks work tiles, heaviest causal tiles first.  A work
+// tile is one (batch*head) and two adjacent 128-row query blocks ("sub-tiles" 0 and
+// 1) that share every K/V block loaded for them.  Inside a CTA the work is split by
+// role:
 //
-//   warp 4      TMA producer: Q tile (double-buffered) and a ring of K/V stages.
-//   warp 5      MMA issuer (one thread): S = Q K^T into tensor memory (double-
-//               buffered), then O += P V with P read from tensor memory.
-//   warps 0-3   softmax warpgroup, one thread per query row: reads its row of S
-//               from tensor memory, applies the causal/tail mask, updates the
-//               running maximum m and running sum l, writes P (16-bit) back to
-//               tensor memory, rescales the unnormalised O when m moved, and in
-//               the epilogue divides O by l and writes O and lse.
+//   warps 0-3   softmax warpgroup of sub-tile 0 (one thread per query row)
+//   warps 4-7   softmax warpgroup of sub-tile 1
+//   warp 8      TMA producer: the Q pair, then a ring of K/V stages
+//   warp 9      MMA issuer (one thread): S_t = Q_t K^T into tensor memory and
+//               O_t += P_t V with P_t read from tensor memory, alternating between
+//               the two sub-tiles so that one sub-tile's softmax overlaps the other
+//               sub-tile's matrix products
+//
+// A softmax thread reads its row of S from tensor memory, masks the causal diagonal
+// and the ragged tail, updates the running maximum m and running sum l, rescales its
+// row of the unnormalised O when m moved, writes P (16-bit) back to tensor memory,
+// and in the epilogue divides O by l and stores O and lse.
 //
 // The method follows the "Flash Attention" chapter (mlx.void.app): section
-// "地基：流式 softmax" for the running (m, l) with the e^{m_old-m_new} patch,
-// "FlashAttention——把整件事分块塞进 SRAM" for the query-outer / key-value-inner tiling
-// in which the score tile never leaves the chip, and "FlashAttention-2" for the
-// deferred division by l and the skipping of tiles wholly above the causal
-// diagonal.  Exponentials are taken in base 2 with scale*log2(e) folded into one
-// FMA (2^{x log2 e} = e^x).
+// "地基：流式 softmax" for the running (m, l) and the e^{m_old-m_new} patch,
+// "FlashAttention——把整件事分块塞进 SRAM" for the query-outer / key-value-inner tiling in
+// which the score tile never leaves the chip, and "FlashAttention-2" for the
+// deferred division by l, the splitting of the sequence into query blocks across
+// the whole chip, and the skipping of tiles wholly above the causal diagonal.
+// Exponentials are taken in base 2 with scale*log2(e) folded into one FMA.
+//
+// Ordering facts the pipeline relies on:
+//  * every sub-tile has one S buffer; the MMA thread issues S_t(j+1) after
+//    O_t += P_t(j) V(j) and commits both to one barrier, so when the softmax sees
+//    S_t(j+1) the previous P.V has already landed in O_t and O_t can be rescaled
+//    without any further wait;
+//  * tcgen05.mma operations issued by one thread execute in issue order (at d = 128
+//    P_t occupies the first 64 columns of S_t's buffer).
 //
 // The running maximum is only moved when a new row maximum exceeds it by more than
 // 8 (base-2 units).  Until then P entries may reach 2^8; the result is unchanged
-// because l and O are accumulated against the same maximum, and O's rescale in
-// tensor memory is skipped on most blocks.
+// because l and O are accumulated against the same maximum, and the O rescale is
+// skipped on most blocks.
 #include <cuda_fp16.h>
 
 #include "internal.h"
@@ -32,8 +46,14 @@
 namespace fa {
 namespace {
 
-constexpr int kTileRows = 128;   // query rows per tile and keys per key/value block
-constexpr int kThreads = 192;    // 4 softmax warps + producer warp + MMA warp
+constexpr int kTileRows = 128;   // query rows per sub-tile and keys per key/value block
+constexpr int kThreads = 384;    // 2 softmax warpgroups + (producer, MMA, 2 idle) warpgroup
+// Register split: the kernel is compiled for kLaunchRegs per thread; the third
+// warpgroup gives registers back so the softmax warpgroups can hold a whole row of S.
+constexpr int kLaunchRegs = 168;
+constexpr int kSoftmaxRegs = 216;
+constexpr int kOtherRegs = 64;
+static_assert((2 * kSoftmaxRegs + kOtherRegs) * 128 <= kLaunchRegs * kThreads, "register split exceeds the launch");
 constexpr int kChunkBytes = kTileRows * 128;   // one 128-row x 128-byte swizzle column block
 constexpr float kRescaleThreshold = 8.0f;
 
@@ -41,36 +61,48 @@ template <int D>
 struct FwdCfg {
   static constexpr int kChunks = D / 64;                    // 64 16-bit elements per 128-byte row
   static constexpr int kTileBytes = kTileRows * D * 2;
+  static constexpr int kQBufs = (D == 64) ? 2 : 1;
   static constexpr int kStages = (D == 64) ? 4 : 2;
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + 2 * kTileBytes;
+  static constexpr int kOffQ = 0;                           // [kQBufs][2 sub-tiles]
+  static constexpr int kOffK = kOffQ + kQBufs * 2 * kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kStages * kTileBytes;
   // barrier indices
-  static constexpr int kQFull = 0;                          // [2]
-  static constexpr int kQEmpty = 2;                         // [2]
-  static constexpr int kKFull = 4;                          // [kStages]
+  static constexpr int kQFull = 0;                          // [kQBufs]
+  static constexpr int kQEmpty = kQFull + kQBufs;           // [kQBufs]
+  static constexpr int kKFull = kQEmpty + kQBufs;           // [kStages]
   static constexpr int kVFull = kKFull + kStages;           // [kStages]
   static constexpr int kKVEmpty = kVFull + kStages;         // [kStages]
   static constexpr int kSFull = kKVEmpty + kStages;         // [2]
   static constexpr int kPFull = kSFull + 2;                 // [2]
-  static constexpr int kPVDone = kPFull + 2;
-  static constexpr int kOEmpty = kPVDone + 1;
-  static constexpr int kDrain = kOEmpty + 1;
+  static constexpr int kOFull = kPFull + 2;                 // [2]
+  static constexpr int kOEmpty = kOFull + 2;                // [2]
+  static constexpr int kDrain = kOEmpty + 2;
   static constexpr int kNumBars = kDrain + 1;
-  // + alignment slack; d = 64 also keeps 32 KB after the last V stage so that every
-  // operand read an MMA descriptor can address stays inside this CTA's allocation
-  static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024 + (D == 64 ? 32768 : 0);
+  static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;   // + alignment slack
   // tensor memory columns (512 allocated)
-  static constexpr uint32_t kTmS = 0;      // S buffers at 0 and 128 (fp32)
-  static constexpr uint32_t kTmP = 256;    // P buffers at 256 and 320 (16-bit pairs)
-  static constexpr uint32_t kTmO = 384;    // O accumulator, D columns (fp32)
+  __host__ __device__ static constexpr uint32_t tm_s(int t) { return t * 128; }
+  __host__ __device__ static constexpr uint32_t tm_p(int t) { return D == 64 ? 256 + t * 64 : t * 128; }
+  __host__ __device__ static constexpr uint32_t tm_o(int t) { return D == 64 ? 384 + t * 64 : 256 + t * 128; }
 };
 
-__device__ __forceinline__ void decode_tile(int tile, int BH, int nqb, int& bh, int& qb) {
-  const int r = tile / BH;   // r = 0 holds the last (heaviest, causal) query block of every head
-  bh = tile - r * BH;
-  qb = nqb - 1 - r;
+struct TileInfo {
+  int bh, qb0, n0, n1, nkv;
+};
+
+// Work tile `tile` -> head, first query block and the key/value block counts of the
+// two sub-tiles (n1 = 0 when the second block lies past the sequence end).
+__device__ __forceinline__ TileInfo decode_tile(int tile, int BH, int nqb, bool causal) {
+  const int npairs = (nqb + 1) >> 1;
+  TileInfo ti;
+  const int r = tile / BH;   // r = 0: the last (heaviest, causal) pair of every head
+  ti.bh = tile - r * BH;
+  const int p = npairs - 1 - r;
+  ti.qb0 = 2 * p;
+  ti.n0 = causal ? ti.qb0 + 1 : nqb;
+  ti.n1 = (ti.qb0 + 1 < nqb) ? (causal ? ti.qb0 + 2 : nqb) : 0;
+  ti.nkv = ti.n0 > ti.n1 ? ti.n0 : ti.n1;
+  return ti;
 }
 
 template <int D, int DT, bool CAUSAL>
@@ -89,27 +121,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int nqb = (N + kTileRows - 1) / kTileRows;
-  const int ntiles = BH * nqb;
+  const int ntiles = BH * ((nqb + 1) >> 1);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::kQBufs; ++i) {
       mbar_init(bar(C::kQFull + i), 1);
       mbar_init(bar(C::kQEmpty + i), 1);
-      mbar_init(bar(C::kSFull + i), 1);
-      mbar_init(bar(C::kPFull + i), kTileRows);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(C::kSFull + t), 1);
+      mbar_init(bar(C::kPFull + t), kTileRows);
+      mbar_init(bar(C::kOFull + t), 1);
+      mbar_init(bar(C::kOEmpty + t), kTileRows);
     }
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(bar(C::kKFull + i), 1);
       mbar_init(bar(C::kVFull + i), 1);
       mbar_init(bar(C::kKVEmpty + i), 1);
     }
-    mbar_init(bar(C::kPVDone), 1);
-    mbar_init(bar(C::kOEmpty), kTileRows);
     mbar_init(bar(C::kDrain), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_holder), 512);
     tmem_relinquish();
   }
@@ -120,7 +154,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtl ctl{abort_flag, err_word, limit_ns};
   const WaitCtl drain{nullptr, err_word, limit_ns};
 
-  if (warp == 4) {
+  if (warp >= 8) {
+    regs_dec<kOtherRegs>();
+  }
+  if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       prefetch_tmap(&tm_q);
@@ -130,20 +167,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++it) {
-        int bh, qb;
-        decode_tile(tile, BH, nqb, bh, qb);
-        const int nkv = CAUSAL ? qb + 1 : nqb;
-        const int qbuf = it & 1;
-        if (it >= 2 && !mbar_wait(bar(C::kQEmpty + qbuf), ((it >> 1) - 1) & 1, ctl, 0x101)) {
+        const TileInfo ti = decode_tile(tile, BH, nqb, CAUSAL);
+        const int qbuf = it % C::kQBufs;
+        if (it >= C::kQBufs &&
+            !mbar_wait(bar(C::kQEmpty + qbuf), ((it / C::kQBufs) - 1) & 1, ctl, 0x101)) {
           ok = false;
           break;
         }
-        const uint32_t qdst = smem_u32(smem + C::kOffQ + qbuf * C::kTileBytes);
-        mbar_arrive_expect_tx(bar(C::kQFull + qbuf), C::kTileBytes);
+        const int nsub = ti.n1 > 0 ? 2 : 1;
+        mbar_arrive_expect_tx(bar(C::kQFull + qbuf), nsub * C::kTileBytes);
+        for (int t = 0; t < nsub; ++t) {
+          const uint32_t qdst = smem_u32(smem + C::kOffQ + (qbuf * 2 + t) * C::kTileBytes);
 #pragma unroll
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(qdst + c * kChunkBytes, &tm_q, bar(C::kQFull + qbuf), c * 64, qb * kTileRows, bh);
-        for (int j = 0; j < nkv; ++j, ++g) {
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d(qdst + c * kChunkBytes, &tm_q, bar(C::kQFull + qbuf), c * 64, (ti.qb0 + t) * kTileRows,
+                        ti.bh);
+        }
+        for (int j = 0; j < ti.nkv; ++j, ++g) {
           const int st = g % C::kStages;
           if (g >= (uint32_t)C::kStages &&
               !mbar_wait(bar(C::kKVEmpty + st), ((g / C::kStages) - 1) & 1, ctl, 0x102)) {
@@ -155,11 +195,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(bar(C::kKFull + st), C::kTileBytes);
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c)
-            tma_load_3d(kdst + c * kChunkBytes, &tm_k, bar(C::kKFull + st), c * 64, j * kTileRows, bh);
+            tma_load_3d(kdst + c * kChunkBytes, &tm_k, bar(C::kKFull + st), c * 64, j * kTileRows, ti.bh);
           mbar_arrive_expect_tx(bar(C::kVFull + st), C::kTileBytes);
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c)
-            tma_load_3d(vdst + c * kChunkBytes, &tm_v, bar(C::kVFull + st), c * 64, j * kTileRows, bh);
+            tma_load_3d(vdst + c * kChunkBytes, &tm_v, bar(C::kVFull + st), c * 64, j * kTileRows, ti.bh);
         }
       }
       // On abort, every copy already issued must land before the CTA exits.
@@ -171,15 +211,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(bar(C::kVFull + st), (last / C::kStages) & 1, drain, 0x1f2);
           }
         }
-        for (int qb2 = 0; qb2 < 2; ++qb2) {
-          if (it > qb2) {
-            const int last = it - 1 - ((it - 1 - qb2) & 1);
-            mbar_wait(bar(C::kQFull + qb2), (last >> 1) & 1, drain, 0x1f3);
+        for (int b = 0; b < C::kQBufs; ++b) {
+          if (it > b) {
+            const int last = it - 1 - ((it - 1 - b) % C::kQBufs);
+            mbar_wait(bar(C::kQFull + b), (last / C::kQBufs) & 1, drain, 0x1f3);
           }
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t ab = (DT == 0) ? 1u : 0u;   // instruction-descriptor code: bf16 = 1, fp16 = 0
@@ -187,164 +227,183 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_pv = idesc_f16(ab, 0, 1, 128, D);
       uint32_t g = 0;
       int it = 0;
+      uint32_t c[2] = {0, 0};   // steps issued per sub-tile (S-full / P-full phases)
+      uint32_t e[2] = {0, 0};   // epilogues per sub-tile (O-full / O-empty phases)
       bool ok = true;
-      auto issue_pv = [&](uint32_t gp, int jp) -> bool {
-        const int sb = gp & 1;
-        const int st = gp % C::kStages;
-        if (!mbar_wait(bar(C::kPFull + sb), (gp >> 1) & 1, ctl, 0x201)) return false;
-        if (!mbar_wait(bar(C::kVFull + st), (gp / C::kStages) & 1, ctl, 0x202)) return false;
-        if (jp == 0 && it > 0 && !mbar_wait(bar(C::kOEmpty), (it - 1) & 1, ctl, 0x203)) return false;
-        tc_fence_after();
-        const uint32_t vbase = smem_u32(smem + C::kOffV + st * C::kTileBytes);
+      auto issue_s = [&](int t, uint32_t qbase, uint32_t kbase) {
 #pragma unroll
-        for (int kk = 0; kk < kTileRows / 16; ++kk) {
-          // B = V (keys x d), d contiguous: MN-major; 16 keys = 16 rows of 128 bytes
-          const uint64_t bdesc = sdesc_sw128(vbase + kk * 16 * 128, kChunkBytes, 1024);
-          umma_ts(tmem + C::kTmO, tmem + C::kTmP + sb * 64 + kk * 8, bdesc, idesc_pv,
-                  (jp > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          // A = Q (rows x d), B = K (keys x d): both K-major; 16 elements = 32 bytes
+          const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+          umma_ss(tmem + C::tm_s(t), sdesc_sw128(qbase + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
+                  idesc_qk, kk > 0 ? 1u : 0u);
         }
-        umma_commit(bar(C::kPVDone));
-        umma_commit(bar(C::kKVEmpty + st));
-        return true;
       };
       for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++it) {
-        int bh, qb;
-        decode_tile(tile, BH, nqb, bh, qb);
-        const int nkv = CAUSAL ? qb + 1 : nqb;
-        const int qbuf = it & 1;
-        if (!mbar_wait(bar(C::kQFull + qbuf), (it >> 1) & 1, ctl, 0x204)) break;
-        const uint32_t qbase = smem_u32(smem + C::kOffQ + qbuf * C::kTileBytes);
-        for (int j = 0; j < nkv; ++j, ++g) {
-          const int st = g % C::kStages;
-          if (!mbar_wait(bar(C::kKFull + st), (g / C::kStages) & 1, ctl, 0x205)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t kbase = smem_u32(smem + C::kOffK + st * C::kTileBytes);
-          const uint32_t d_s = tmem + C::kTmS + (g & 1) * 128;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            // A = Q (rows x d), B = K (keys x d): both K-major; 16 elements = 32 bytes
-            const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-            umma_ss(d_s, sdesc_sw128(qbase + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024), idesc_qk,
-                    kk > 0 ? 1u : 0u);
-          }
-          umma_commit(bar(C::kSFull + (g & 1)));
-          if (j == nkv - 1) umma_commit(bar(C::kQEmpty + qbuf));
-          if (j > 0 && !issue_pv(g - 1, j - 1)) {
-            ok = false;
-            break;
+        const TileInfo ti = decode_tile(tile, BH, nqb, CAUSAL);
+        const int n[2] = {ti.n0, ti.n1};
+        const int qbuf = it % C::kQBufs;
+        const uint32_t qbase0 = smem_u32(smem + C::kOffQ + (qbuf * 2) * C::kTileBytes);
+        if (!mbar_wait(bar(C::kQFull + qbuf), (it / C::kQBufs) & 1, ctl, 0x201)) break;
+        if (!mbar_wait(bar(C::kKFull + g % C::kStages), (g / C::kStages) & 1, ctl, 0x202)) break;
+        tc_fence_after();
+        {
+          const uint32_t kbase = smem_u32(smem + C::kOffK + (g % C::kStages) * C::kTileBytes);
+          for (int t = 0; t < 2; ++t) {
+            if (n[t] == 0) continue;
+            issue_s(t, qbase0 + t * C::kTileBytes, kbase);
+            umma_commit(bar(C::kSFull + t));
           }
         }
-        if (ok && !issue_pv(g - 1, nkv - 1)) ok = false;
+        for (int j = 0; ok && j < ti.nkv; ++j) {
+          const uint32_t gj = g + j;
+          const int st = gj % C::kStages;
+          const int stn = (gj + 1) % C::kStages;
+          if (j + 1 < ti.nkv && !mbar_wait(bar(C::kKFull + stn), ((gj + 1) / C::kStages) & 1, ctl, 0x203)) {
+            ok = false;
+            break;
+          }
+          if (!mbar_wait(bar(C::kVFull + st), (gj / C::kStages) & 1, ctl, 0x204)) {
+            ok = false;
+            break;
+          }
+          const uint32_t vbase = smem_u32(smem + C::kOffV + st * C::kTileBytes);
+          const uint32_t knext = smem_u32(smem + C::kOffK + stn * C::kTileBytes);
+          for (int t = 0; t < 2; ++t) {
+            if (j >= n[t]) continue;
+            if (!mbar_wait(bar(C::kPFull + t), c[t] & 1, ctl, 0x205) ||
+                (j == 0 && e[t] > 0 && !mbar_wait(bar(C::kOEmpty + t), (e[t] - 1) & 1, ctl, 0x206))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < kTileRows / 16; ++kk) {
+              // B = V (keys x d), d contiguous: MN-major; 16 keys = 16 rows of 128 bytes
+              const uint64_t bdesc = sdesc_sw128(vbase + kk * 16 * 128, kChunkBytes, 1024);
+              umma_ts(tmem + C::tm_o(t), tmem + C::tm_p(t) + kk * 8, bdesc, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            if (j + 1 < n[t]) {
+              issue_s(t, qbase0 + t * C::kTileBytes, knext);
+              umma_commit(bar(C::kSFull + t));
+            } else {
+              umma_commit(bar(C::kOFull + t));
+              ++e[t];
+            }
+            ++c[t];
+          }
+          if (ok) umma_commit(bar(C::kKVEmpty + st));
+        }
+        if (!ok) break;
+        umma_commit(bar(C::kQEmpty + qbuf));
+        g += ti.nkv;
       }
       // no MMA may still be running on tensor memory when the CTA tears down
       umma_commit(bar(C::kDrain));
       mbar_wait(bar(C::kDrain), 0, drain, 0x2f1);
     }
-  } else {
-    // ------------------------------------------------------------ softmax warpgroup
-    const int t = threadIdx.x;                       // row inside the tile
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    uint32_t g = 0;
-    uint32_t pv_phase = 0;                           // completed PV-done phases waited so far
-    int it = 0;
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
-      int bh, qb;
-      decode_tile(tile, BH, nqb, bh, qb);
-      const int nkv = CAUSAL ? qb + 1 : nqb;
-      const int row = qb * kTileRows + t;
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ softmax warpgroups
+    regs_inc<kSoftmaxRegs>();
+    const int t = warp >> 2;                          // sub-tile of this warpgroup
+    const int tid = threadIdx.x & 127;                // row inside the sub-tile
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t s_addr = tmem + lane_base + C::tm_s(t);
+    const uint32_t p_addr = tmem + lane_base + C::tm_p(t);
+    const uint32_t o_addr = tmem + lane_base + C::tm_o(t);
+    const uint64_t c2 = f2_pack(scale_log2, scale_log2);
+    uint32_t c = 0;   // steps of this sub-tile (S-full / P-full phases)
+    uint32_t e = 0;   // epilogues of this sub-tile
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+      const TileInfo ti = decode_tile(tile, BH, nqb, CAUSAL);
+      const int n = t == 0 ? ti.n0 : ti.n1;
+      if (n == 0) continue;
+      const int qb = ti.qb0 + t;
+      const int row = qb * kTileRows + tid;
       float m = -INFINITY;
       float l = 0.f;
       bool ok = true;
-      for (int j = 0; j < nkv; ++j, ++g) {
-        const int sb = g & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kSFull + sb), (g >> 1) & 1, ctl, 0x301))) {
+      for (int j = 0; j < n; ++j, ++c) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kSFull + t), c & 1, ctl, 0x301))) {
           ok = false;
           break;
         }
         tc_fence_after();
         uint32_t sr[128];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_base + C::kTmS + sb * 128 + c * 32, sr + c * 32);
+        for (int q = 0; q < 4; ++q) tmem_ld32(s_addr + q * 32, sr + q * 32);
         tmem_ld_wait();
         reg_fence<128>(sr);
         float* s = reinterpret_cast<float*>(sr);
         const int kbase = j * kTileRows;
-        const bool tail = (kbase + kTileRows > N);
-        const bool diag = CAUSAL && (j == qb);
-        if (tail || diag) {
+        if ((kbase + kTileRows > N) || (CAUSAL && j == qb)) {
           const int lim = CAUSAL ? min(N - 1, row) : (N - 1);   // last visible key
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (kbase + c > lim) s[c] = -INFINITY;
+          for (int q = 0; q < 128; ++q)
+            if (kbase + q > lim) s[q] = -INFINITY;
         }
-        // row maximum: 8 independent chains, then a tree
-        float m8[8];
+        // row maximum: three-input max tree
+        float m3[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) m8[i] = s[i];
+        for (int i = 0; i < 8; ++i) m3[i] = fmax3(s[i], s[8 + i], s[16 + i]);
 #pragma unroll
-        for (int c = 8; c < 128; c += 8)
+        for (int q = 24; q < 120; q += 16)
 #pragma unroll
-          for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], s[c + i]);
-        const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+          for (int i = 0; i < 8; ++i) m3[i] = fmax3(m3[i], s[q + i], s[q + 8 + i]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m3[i] = fmaxf(m3[i], s[120 + i]);
+        const float mx = fmax3(fmax3(m3[0], m3[1], m3[2]), fmax3(m3[3], m3[4], m3[5]), fmaxf(m3[6], m3[7]));
         const float mc = mx * scale_log2;
         const float m_new = (mc > m + kRescaleThreshold) ? mc : m;
         const float alpha = ex2_approx(m - m_new);
-        const float neg_m = -m_new;
-        float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        const uint64_t nm2 = f2_pack(-m_new, -m_new);
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
         uint32_t pk[64];
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float p0 = ex2_approx(fmaf(s[2 * c], scale_log2, neg_m));
-          const float p1 = ex2_approx(fmaf(s[2 * c + 1], scale_log2, neg_m));
-          l8[(2 * c) & 7] += p0;
-          l8[(2 * c + 1) & 7] += p1;
-          pk[c] = pack2<DT>(p0, p1);
+        for (int q = 0; q < 64; ++q) {
+          float x0, x1;
+          f2_unpack(ffma2(f2_pack(s[2 * q], s[2 * q + 1]), c2, nm2), x0, x1);
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
+          acc[q & 3] = fadd2(acc[q & 3], f2_pack(p0, p1));
+          pk[q] = pack2<DT>(p0, p1);
         }
-        const float rowsum = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+        tmem_st32(p_addr, pk);
+        tmem_st32(p_addr + 32, pk + 32);
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+          // O holds every earlier P.V (committed before this S); bring it to the new maximum
+#pragma unroll
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t orr[32];
+            tmem_ld32(o_addr + q * 32, orr);
+            tmem_ld_wait();
+            reg_fence<32>(orr);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+            tmem_st32(o_addr + q * 32, orr);
+          }
+        }
+        float a0, a1, b0, b1;
+        f2_unpack(fadd2(acc[0], acc[1]), a0, a1);
+        f2_unpack(fadd2(acc[2], acc[3]), b0, b1);
+        const float rowsum = (a0 + a1) + (b0 + b1);
         l = l * alpha + rowsum;
-        tmem_st32(tmem + lane_base + C::kTmP + sb * 64, pk);
-        tmem_st32(tmem + lane_base + C::kTmP + sb * 64 + 32, pk + 32);
-        if (j > 0) {
-          // the previous P.V must have landed in O before O is rescaled
-          if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kPVDone), pv_phase & 1, ctl, 0x302))) {
-            ok = false;
-            break;
-          }
-          ++pv_phase;
-          tc_fence_after();
-          if (__any_sync(0xffffffffu, alpha != 1.0f)) {
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t orr[32];
-              tmem_ld32(tmem + lane_base + C::kTmO + c * 32, orr);
-              tmem_ld_wait();
-              reg_fence<32>(orr);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
-              tmem_st32(tmem + lane_base + C::kTmO + c * 32, orr);
-            }
-          }
-        }
+        m = m_new;
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(bar(C::kPFull + sb));
-        m = m_new;
+        mbar_arrive(bar(C::kPFull + t));
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kPVDone), pv_phase & 1, ctl, 0x303))) break;
-      ++pv_phase;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kOFull + t), e & 1, ctl, 0x303))) break;
+      ++e;
       tc_fence_after();
       const float inv_l = 1.0f / l;
-      uint8_t* orow = reinterpret_cast<uint8_t*>(out) + ((size_t)bh * N + row) * (D * 2);
+      uint8_t* orow = reinterpret_cast<uint8_t*>(out) + ((size_t)ti.bh * N + row) * (D * 2);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int q = 0; q < D / 32; ++q) {
         uint32_t orr[32];
-        tmem_ld32(tmem + lane_base + C::kTmO + c * 32, orr);
+        tmem_ld32(o_addr + q * 32, orr);
         tmem_ld_wait();
         reg_fence<32>(orr);
         uint32_t w[16];
@@ -353,19 +412,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           w[i] = pack2<DT>(__uint_as_float(orr[2 * i]) * inv_l, __uint_as_float(orr[2 * i + 1]) * inv_l);
         if (row < N) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) st_global_v4(orow + c * 64 + i * 16, w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          for (int i = 0; i < 4; ++i)
+            st_global_v4(orow + q * 64 + i * 16, w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
         }
       }
-      if (row < N) lse[(size_t)bh * N + row] = (m + lg2_approx(l)) * 0.69314718055994530942f;
+      if (row < N) lse[(size_t)ti.bh * N + row] = (m + lg2_approx(l)) * 0.69314718055994530942f;
       tc_fence_before();
-      mbar_arrive(bar(C::kOEmpty));
+      mbar_arrive(bar(C::kOEmpty + t));
     }
   }
 
   // ------------------------------------------------------------ teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -377,8 +437,14 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   auto kern = fwd_kernel<D, DT, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
+  // The register split inside the kernel must fit what the launch provides, or the
+  // softmax warpgroups' setmaxnreg.inc would never be granted.
+  cudaFuncAttributes attr;
+  e = cudaFuncGetAttributes(&attr, kern);
+  if (e != cudaSuccess) return e;
+  if (attr.numRegs * kThreads < (2 * kSoftmaxRegs + kOtherRegs) * 128) return cudaErrorInvalidConfiguration;
   const int nqb = (a.N + kTileRows - 1) / kTileRows;
-  const int ntiles = a.BH * nqb;
+  const int ntiles = a.BH * ((nqb + 1) / 2);
   const int grid = ntiles < a.num_sms ? ntiles : a.num_sms;
   kern<<<grid, kThreads, C::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, static_cast<uint16_t*>(a.o), a.lse,
                                                    a.BH, a.N, a.scale_log2, a.err_word, a.limit_ns);
