@@ -118,8 +118,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   auto bar = [&](int i) { return smem_u32(bars + i); };
 
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
+  // warp index through a shuffle so the compiler can treat it (and every TMEM
+  // address, descriptor and loop bound derived from it) as warp-uniform
+  const int warp = __shfl_sync(0xffffffffu, threadIdx.x >> 5, 0);
   const int nqb = (N + kTileRows - 1) / kTileRows;
   const int ntiles = BH * ((nqb + 1) >> 1);
 
@@ -158,48 +159,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_dec<kOtherRegs>();
   }
   if (warp == 8) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      prefetch_tmap(&tm_q);
-      prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_v);
+    // ------------------------------------------------------------ TMA producer (whole warp; one lane issues)
+    {
+      if (elect_one()) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+      }
       uint32_t g = 0;
       int it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++it) {
         const TileInfo ti = decode_tile(tile, BH, nqb, CAUSAL);
         const int qbuf = it % C::kQBufs;
-        if (it >= C::kQBufs &&
-            !mbar_wait(bar(C::kQEmpty + qbuf), ((it / C::kQBufs) - 1) & 1, ctl, 0x101)) {
+        if (it >= C::kQBufs && !wait_warp(bar(C::kQEmpty + qbuf), ((it / C::kQBufs) - 1) & 1, ctl, 0x101)) {
           ok = false;
           break;
         }
         const int nsub = ti.n1 > 0 ? 2 : 1;
-        mbar_arrive_expect_tx(bar(C::kQFull + qbuf), nsub * C::kTileBytes);
-        for (int t = 0; t < nsub; ++t) {
-          const uint32_t qdst = smem_u32(smem + C::kOffQ + (qbuf * 2 + t) * C::kTileBytes);
+        if (elect_one()) {
+          mbar_arrive_expect_tx(bar(C::kQFull + qbuf), nsub * C::kTileBytes);
+          for (int t = 0; t < nsub; ++t) {
+            const uint32_t qdst = smem_u32(smem + C::kOffQ + (qbuf * 2 + t) * C::kTileBytes);
 #pragma unroll
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_load_3d(qdst + c * kChunkBytes, &tm_q, bar(C::kQFull + qbuf), c * 64, (ti.qb0 + t) * kTileRows,
-                        ti.bh);
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_3d(qdst + c * kChunkBytes, &tm_q, bar(C::kQFull + qbuf), c * 64, (ti.qb0 + t) * kTileRows,
+                          ti.bh);
+          }
         }
+        __syncwarp();
         for (int j = 0; j < ti.nkv; ++j, ++g) {
           const int st = g % C::kStages;
           if (g >= (uint32_t)C::kStages &&
-              !mbar_wait(bar(C::kKVEmpty + st), ((g / C::kStages) - 1) & 1, ctl, 0x102)) {
+              !wait_warp(bar(C::kKVEmpty + st), ((g / C::kStages) - 1) & 1, ctl, 0x102)) {
             ok = false;
             break;
           }
           const uint32_t kdst = smem_u32(smem + C::kOffK + st * C::kTileBytes);
           const uint32_t vdst = smem_u32(smem + C::kOffV + st * C::kTileBytes);
-          mbar_arrive_expect_tx(bar(C::kKFull + st), C::kTileBytes);
+          if (elect_one()) {
+            mbar_arrive_expect_tx(bar(C::kKFull + st), C::kTileBytes);
 #pragma unroll
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_load_3d(kdst + c * kChunkBytes, &tm_k, bar(C::kKFull + st), c * 64, j * kTileRows, ti.bh);
-          mbar_arrive_expect_tx(bar(C::kVFull + st), C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_3d(kdst + c * kChunkBytes, &tm_k, bar(C::kKFull + st), c * 64, j * kTileRows, ti.bh);
+            mbar_arrive_expect_tx(bar(C::kVFull + st), C::kTileBytes);
 #pragma unroll
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_load_3d(vdst + c * kChunkBytes, &tm_v, bar(C::kVFull + st), c * 64, j * kTileRows, ti.bh);
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_3d(vdst + c * kChunkBytes, &tm_v, bar(C::kVFull + st), c * 64, j * kTileRows, ti.bh);
+          }
+          __syncwarp();
         }
       }
       // On abort, every copy already issued must land before the CTA exits.
@@ -220,8 +228,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (whole warp; one lane issues)
+    {
       constexpr uint32_t ab = (DT == 0) ? 1u : 0u;   // instruction-descriptor code: bf16 = 1, fp16 = 0
       constexpr uint32_t idesc_qk = idesc_f16(ab, 0, 0, 128, 128);
       constexpr uint32_t idesc_pv = idesc_f16(ab, 0, 1, 128, D);
@@ -231,12 +239,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t e[2] = {0, 0};   // epilogues per sub-tile (O-full / O-empty phases)
       bool ok = true;
       auto issue_s = [&](int t, uint32_t qbase, uint32_t kbase) {
+        const uint64_t qd = sdesc_sw128(qbase, 16, 1024);
+        const uint64_t kd = sdesc_sw128(kbase, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           // A = Q (rows x d), B = K (keys x d): both K-major; 16 elements = 32 bytes
-          const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-          umma_ss(tmem + C::tm_s(t), sdesc_sw128(qbase + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
-                  idesc_qk, kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
+          umma_ss(tmem + C::tm_s(t), qd + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
         }
       };
       for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++it) {
@@ -244,26 +253,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n[2] = {ti.n0, ti.n1};
         const int qbuf = it % C::kQBufs;
         const uint32_t qbase0 = smem_u32(smem + C::kOffQ + (qbuf * 2) * C::kTileBytes);
-        if (!mbar_wait(bar(C::kQFull + qbuf), (it / C::kQBufs) & 1, ctl, 0x201)) break;
-        if (!mbar_wait(bar(C::kKFull + g % C::kStages), (g / C::kStages) & 1, ctl, 0x202)) break;
+        if (!wait_warp(bar(C::kQFull + qbuf), (it / C::kQBufs) & 1, ctl, 0x201)) break;
+        if (!wait_warp(bar(C::kKFull + g % C::kStages), (g / C::kStages) & 1, ctl, 0x202)) break;
         tc_fence_after();
         {
           const uint32_t kbase = smem_u32(smem + C::kOffK + (g % C::kStages) * C::kTileBytes);
-          for (int t = 0; t < 2; ++t) {
-            if (n[t] == 0) continue;
-            issue_s(t, qbase0 + t * C::kTileBytes, kbase);
-            umma_commit(bar(C::kSFull + t));
+          if (elect_one()) {
+            for (int t = 0; t < 2; ++t) {
+              if (n[t] == 0) continue;
+              issue_s(t, qbase0 + t * C::kTileBytes, kbase);
+              umma_commit(bar(C::kSFull + t));
+            }
           }
+          __syncwarp();
         }
         for (int j = 0; ok && j < ti.nkv; ++j) {
           const uint32_t gj = g + j;
           const int st = gj % C::kStages;
           const int stn = (gj + 1) % C::kStages;
-          if (j + 1 < ti.nkv && !mbar_wait(bar(C::kKFull + stn), ((gj + 1) / C::kStages) & 1, ctl, 0x203)) {
+          if (j + 1 < ti.nkv && !wait_warp(bar(C::kKFull + stn), ((gj + 1) / C::kStages) & 1, ctl, 0x203)) {
             ok = false;
             break;
           }
-          if (!mbar_wait(bar(C::kVFull + st), (gj / C::kStages) & 1, ctl, 0x204)) {
+          if (!wait_warp(bar(C::kVFull + st), (gj / C::kStages) & 1, ctl, 0x204)) {
             ok = false;
             break;
           }
@@ -271,35 +283,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t knext = smem_u32(smem + C::kOffK + stn * C::kTileBytes);
           for (int t = 0; t < 2; ++t) {
             if (j >= n[t]) continue;
-            if (!mbar_wait(bar(C::kPFull + t), c[t] & 1, ctl, 0x205) ||
-                (j == 0 && e[t] > 0 && !mbar_wait(bar(C::kOEmpty + t), (e[t] - 1) & 1, ctl, 0x206))) {
+            if (!wait_warp(bar(C::kPFull + t), c[t] & 1, ctl, 0x205) ||
+                (j == 0 && e[t] > 0 && !wait_warp(bar(C::kOEmpty + t), (e[t] - 1) & 1, ctl, 0x206))) {
               ok = false;
               break;
             }
             tc_fence_after();
+            if (elect_one()) {
+              const uint64_t vd = sdesc_sw128(vbase, kChunkBytes, 1024);
 #pragma unroll
-            for (int kk = 0; kk < kTileRows / 16; ++kk) {
-              // B = V (keys x d), d contiguous: MN-major; 16 keys = 16 rows of 128 bytes
-              const uint64_t bdesc = sdesc_sw128(vbase + kk * 16 * 128, kChunkBytes, 1024);
-              umma_ts(tmem + C::tm_o(t), tmem + C::tm_p(t) + kk * 8, bdesc, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = 0; kk < kTileRows / 16; ++kk) {
+                // B = V (keys x d), d contiguous: MN-major; 16 keys = 16 rows of 128 bytes
+                umma_ts(tmem + C::tm_o(t), tmem + C::tm_p(t) + kk * 8, vd + ((kk * 16 * 128) >> 4), idesc_pv,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+              }
+              if (j + 1 < n[t]) {
+                issue_s(t, qbase0 + t * C::kTileBytes, knext);
+                umma_commit(bar(C::kSFull + t));
+              } else {
+                umma_commit(bar(C::kOFull + t));
+              }
             }
-            if (j + 1 < n[t]) {
-              issue_s(t, qbase0 + t * C::kTileBytes, knext);
-              umma_commit(bar(C::kSFull + t));
-            } else {
-              umma_commit(bar(C::kOFull + t));
-              ++e[t];
-            }
+            __syncwarp();
+            if (j + 1 >= n[t]) ++e[t];
             ++c[t];
           }
-          if (ok) umma_commit(bar(C::kKVEmpty + st));
+          if (ok && elect_one()) umma_commit(bar(C::kKVEmpty + st));
+          __syncwarp();
         }
         if (!ok) break;
-        umma_commit(bar(C::kQEmpty + qbuf));
+        if (elect_one()) umma_commit(bar(C::kQEmpty + qbuf));
+        __syncwarp();
         g += ti.nkv;
       }
       // no MMA may still be running on tensor memory when the CTA tears down
-      umma_commit(bar(C::kDrain));
+      if (elect_one()) umma_commit(bar(C::kDrain));
+      __syncwarp();
       mbar_wait(bar(C::kDrain), 0, drain, 0x2f1);
     }
   } else if (warp < 8) {

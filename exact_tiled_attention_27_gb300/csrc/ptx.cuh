@@ -101,6 +101,11 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   }
 }
 
+// Bounded wait by a whole warp; the result is the same in every lane.
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const WaitCtl& ctl, uint32_t site) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, ctl, site));
+}
+
 // ------------------------------------------------------------------ fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
