@@ -100,8 +100,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   auto bar = [&](int i) { return smem_u32(bars + i); };
 
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
+  // warp index through a shuffle so the compiler can treat it as warp-uniform
+  const int warp = __shfl_sync(0xffffffffu, threadIdx.x >> 5, 0);
   const int nb = (N + kRows - 1) / kRows;
   const int ntiles = BH * nb;
 
@@ -137,12 +137,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const WaitCtl drain{nullptr, err_word, limit_ns};
 
   if (warp == 8) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      prefetch_tmap(&tm_q);
-      prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_v);
-      prefetch_tmap(&tm_do);
+    // ------------------------------------------------------------ TMA producer (whole warp; one lane issues)
+    {
+      if (elect_one()) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_do);
+      }
       uint32_t s = 0;
       int it = 0;
       bool ok = true;
@@ -151,38 +153,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         decode_kv_tile(tile, BH, nb, CAUSAL, bh, kb);
         const int kvb = it % C::kKVBufs;
         if (it >= C::kKVBufs &&
-            !mbar_wait(bar(C::kKVEmpty + kvb), ((it / C::kKVBufs) - 1) & 1, ctl, 0x401)) {
+            !wait_warp(bar(C::kKVEmpty + kvb), ((it / C::kKVBufs) - 1) & 1, ctl, 0x401)) {
           ok = false;
           break;
         }
         const uint32_t kdst = smem_u32(smem + C::kOffK + kvb * C::kTileBytes);
         const uint32_t vdst = smem_u32(smem + C::kOffV + kvb * C::kTileBytes);
-        mbar_arrive_expect_tx(bar(C::kKVFull + kvb), 2 * C::kTileBytes);
+        if (elect_one()) {
+          mbar_arrive_expect_tx(bar(C::kKVFull + kvb), 2 * C::kTileBytes);
 #pragma unroll
-        for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_3d(kdst + c * kChunkBytes, &tm_k, bar(C::kKVFull + kvb), c * 64, kb * kRows, bh);
-          tma_load_3d(vdst + c * kChunkBytes, &tm_v, bar(C::kKVFull + kvb), c * 64, kb * kRows, bh);
+          for (int c = 0; c < C::kChunks; ++c) {
+            tma_load_3d(kdst + c * kChunkBytes, &tm_k, bar(C::kKVFull + kvb), c * 64, kb * kRows, bh);
+            tma_load_3d(vdst + c * kChunkBytes, &tm_v, bar(C::kKVFull + kvb), c * 64, kb * kRows, bh);
+          }
         }
+        __syncwarp();
         const int q0 = CAUSAL ? kb : 0;
         for (int qi = q0; qi < nb; ++qi, ++s) {
           const int qs = s % C::kQBufs;
           if (s >= (uint32_t)C::kQBufs &&
-              !mbar_wait(bar(C::kQEmpty + qs), ((s / C::kQBufs) - 1) & 1, ctl, 0x402)) {
+              !wait_warp(bar(C::kQEmpty + qs), ((s / C::kQBufs) - 1) & 1, ctl, 0x402)) {
             ok = false;
             break;
           }
           const uint32_t qdst = smem_u32(smem + C::kOffQ + qs * C::kTileBytes);
           const uint32_t odst = smem_u32(smem + C::kOffDO + qs * C::kTileBytes);
           const uint32_t stats = smem_u32(smem + C::kOffStats + qs * 2 * kRows * 4);
-          mbar_arrive_expect_tx(bar(C::kQFull + qs), 2 * C::kTileBytes + 2 * kRows * 4);
+          if (elect_one()) {
+            mbar_arrive_expect_tx(bar(C::kQFull + qs), 2 * C::kTileBytes + 2 * kRows * 4);
 #pragma unroll
-          for (int c = 0; c < C::kChunks; ++c) {
-            tma_load_3d(qdst + c * kChunkBytes, &tm_q, bar(C::kQFull + qs), c * 64, qi * kRows, bh);
-            tma_load_3d(odst + c * kChunkBytes, &tm_do, bar(C::kQFull + qs), c * 64, qi * kRows, bh);
+            for (int c = 0; c < C::kChunks; ++c) {
+              tma_load_3d(qdst + c * kChunkBytes, &tm_q, bar(C::kQFull + qs), c * 64, qi * kRows, bh);
+              tma_load_3d(odst + c * kChunkBytes, &tm_do, bar(C::kQFull + qs), c * 64, qi * kRows, bh);
+            }
+            const size_t srow = (size_t)bh * Npad + (size_t)qi * kRows;
+            bulk_load(stats, lse2 + srow, kRows * 4, bar(C::kQFull + qs));
+            bulk_load(stats + kRows * 4, dvec + srow, kRows * 4, bar(C::kQFull + qs));
           }
-          const size_t srow = (size_t)bh * Npad + (size_t)qi * kRows;
-          bulk_load(stats, lse2 + srow, kRows * 4, bar(C::kQFull + qs));
-          bulk_load(stats + kRows * 4, dvec + srow, kRows * 4, bar(C::kQFull + qs));
+          __syncwarp();
         }
       }
       if (!ok) {
@@ -200,8 +208,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
   } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (whole warp; one lane issues)
+    {
       constexpr uint32_t ab = (DT == 0) ? 1u : 0u;
       constexpr uint32_t idesc_s = idesc_f16(ab, 0, 0, 128, 128);    // A, B K-major
       constexpr uint32_t idesc_kv = idesc_f16(ab, 0, 1, 128, D);     // A K-major, B MN-major
@@ -215,76 +223,86 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         int bh, kb;
         decode_kv_tile(tile, BH, nb, CAUSAL, bh, kb);
         const int kvb = it % C::kKVBufs;
-        if (!mbar_wait(bar(C::kKVFull + kvb), (it / C::kKVBufs) & 1, ctl, 0x501)) break;
+        if (!wait_warp(bar(C::kKVFull + kvb), (it / C::kKVBufs) & 1, ctl, 0x501)) break;
         const uint32_t kbase = smem_u32(smem + C::kOffK + kvb * C::kTileBytes);
         const uint32_t vbase = smem_u32(smem + C::kOffV + kvb * C::kTileBytes);
         const int q0 = CAUSAL ? kb : 0;
         for (int qi = q0; qi < nb; ++qi, ++s) {
           const int qs = s % C::kQBufs;
-          if (!mbar_wait(bar(C::kQFull + qs), (s / C::kQBufs) & 1, ctl, 0x502)) {
+          if (!wait_warp(bar(C::kQFull + qs), (s / C::kQBufs) & 1, ctl, 0x502)) {
             ok = false;
             break;
           }
           // the dQ columns (and, at d = 128, the S^T columns they share) must be drained
-          if (s > 0 && !mbar_wait(bar(C::kDQFree), (s - 1) & 1, ctl, 0x503)) {
+          if (s > 0 && !wait_warp(bar(C::kDQFree), (s - 1) & 1, ctl, 0x503)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t qbase = smem_u32(smem + C::kOffQ + qs * C::kTileBytes);
           const uint32_t obase = smem_u32(smem + C::kOffDO + qs * C::kTileBytes);
+          if (elect_one()) {
+            const uint64_t kd = sdesc_sw128(kbase, 16, 1024), qd = sdesc_sw128(qbase, 16, 1024);
+            const uint64_t vd = sdesc_sw128(vbase, 16, 1024), od = sdesc_sw128(obase, 16, 1024);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-            umma_ss(tmem + C::kTmST, sdesc_sw128(kbase + off, 16, 1024), sdesc_sw128(qbase + off, 16, 1024),
-                    idesc_s, kk > 0 ? 1u : 0u);
-          }
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
+              umma_ss(tmem + C::kTmST, kd + off, qd + off, idesc_s, kk > 0 ? 1u : 0u);
+            }
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-            umma_ss(tmem + C::kTmDPT, sdesc_sw128(vbase + off, 16, 1024), sdesc_sw128(obase + off, 16, 1024),
-                    idesc_s, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
+              umma_ss(tmem + C::kTmDPT, vd + off, od + off, idesc_s, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(bar(C::kSFull));
           }
-          umma_commit(bar(C::kSFull));
-          if (!mbar_wait(bar(C::kDSFull), s & 1, ctl, 0x504)) {
+          __syncwarp();
+          if (!wait_warp(bar(C::kDSFull), s & 1, ctl, 0x504)) {
             ok = false;
             break;
           }
-          if (qi == q0 && it > 0 && !mbar_wait(bar(C::kDKVEmpty), (it - 1) & 1, ctl, 0x505)) {
+          if (qi == q0 && it > 0 && !wait_warp(bar(C::kDKVEmpty), (it - 1) & 1, ctl, 0x505)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t first = (qi == q0) ? 1u : 0u;
+          if (elect_one()) {
+            const uint64_t ptk = sdesc_sw128(pt, 16, 1024), dsk = sdesc_sw128(dst, 16, 1024);
+            const uint64_t omn = sdesc_sw128(obase, kChunkBytes, 1024), qmn = sdesc_sw128(qbase, kChunkBytes, 1024);
+            const uint64_t dsmn = sdesc_sw128(dst, kChunkBytes, 1024), kmn = sdesc_sw128(kbase, kChunkBytes, 1024);
 #pragma unroll
-          for (int kk = 0; kk < kRows / 16; ++kk) {
-            // A = P^T / dS^T (keys x q, q contiguous): K-major, 16 q = 32 bytes
-            const uint32_t aoff = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-            // B = dO / Q (q x d, d contiguous): MN-major, 16 q = 16 rows of 128 bytes
-            const uint32_t boff = kk * 16 * 128;
-            const uint32_t acc = (first && kk == 0) ? 0u : 1u;
-            umma_ss(tmem + C::kTmDV, sdesc_sw128(pt + aoff, 16, 1024), sdesc_sw128(obase + boff, kChunkBytes, 1024),
-                    idesc_kv, acc);
-            umma_ss(tmem + C::kTmDK, sdesc_sw128(dst + aoff, 16, 1024), sdesc_sw128(qbase + boff, kChunkBytes, 1024),
-                    idesc_kv, acc);
-          }
+            for (int kk = 0; kk < kRows / 16; ++kk) {
+              // A = P^T / dS^T (keys x q, q contiguous): K-major, 16 q = 32 bytes
+              const uint32_t aoff = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
+              // B = dO / Q (q x d, d contiguous): MN-major, 16 q = 16 rows of 128 bytes
+              const uint32_t boff = (kk * 16 * 128) >> 4;
+              const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+              umma_ss(tmem + C::kTmDV, ptk + aoff, omn + boff, idesc_kv, acc);
+              umma_ss(tmem + C::kTmDK, dsk + aoff, qmn + boff, idesc_kv, acc);
+            }
 #pragma unroll
-          for (int kk = 0; kk < kRows / 16; ++kk) {
-            // A = dS (q x keys) read from the dS^T block: MN-major, 16 keys = 16 rows
-            // B = K (keys x d, d contiguous): MN-major, 16 keys = 16 rows
-            const uint32_t off = kk * 16 * 128;
-            umma_ss(tmem + C::kTmDQ, sdesc_sw128(dst + off, kChunkBytes, 1024),
-                    sdesc_sw128(kbase + off, kChunkBytes, 1024), idesc_q, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < kRows / 16; ++kk) {
+              // A = dS (q x keys) read from the dS^T block: MN-major, 16 keys = 16 rows
+              // B = K (keys x d, d contiguous): MN-major, 16 keys = 16 rows
+              const uint32_t off = (kk * 16 * 128) >> 4;
+              umma_ss(tmem + C::kTmDQ, dsmn + off, kmn + off, idesc_q, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(bar(C::kMmaDone));
+            umma_commit(bar(C::kQEmpty + qs));
+            umma_commit(bar(C::kDQFull));
           }
-          umma_commit(bar(C::kMmaDone));
-          umma_commit(bar(C::kQEmpty + qs));
-          umma_commit(bar(C::kDQFull));
+          __syncwarp();
         }
         if (!ok) break;
-        umma_commit(bar(C::kKVEmpty + kvb));
-        umma_commit(bar(C::kDKVFull));
+        if (elect_one()) {
+          umma_commit(bar(C::kKVEmpty + kvb));
+          umma_commit(bar(C::kDKVFull));
+        }
+        __syncwarp();
       }
-      umma_commit(bar(C::kDrain));
+      if (elect_one()) umma_commit(bar(C::kDrain));
+      __syncwarp();
       mbar_wait(bar(C::kDrain), 0, drain, 0x5f1);
     }
   } else if (warp < 4) {
