@@ -9,18 +9,32 @@
 //   dQ = scale dS K,  dK = scale dS^T Q.
 //
 // Three launches:
-//   bwd_pre_kernel   D and lse*log2(e) per row, padded to whole 128-row blocks
-//                    (padding rows get D = 0 and +inf, so their P is exactly 0);
+//   bwd_pre_kernel   -D and -lse*log2(e) per row, padded to whole 128-row blocks
+//                    (padding rows get 0 and -inf, so their P is exactly 0);
 //                    zeroes the float32 dQ accumulator.
 //   bwd_kv_kernel    persistent over (batch*head, 128-key block) tiles, key/value
 //                    block on the outside, query blocks inside.  Per query block:
 //                      S^T = K Q^T, dP^T = V dO^T            (tcgen05, tensor memory)
 //                      P^T = 2^(S^T scale log2e - lse2), dS^T = P^T o (dP^T - D)
-//                                                            (one thread per key row)
-//                      dV += P^T dO, dK += dS^T Q, dQ_part = dS K
+//                                        (one thread per key row and query half)
+//                      dV += P^T dO      (P^T read from tensor memory)
+//                      dK += dS^T Q, dQ_part = dS K      (dS^T from shared memory)
 //                    dQ_part is added into the float32 accumulator with vector
 //                    reductions; dK (times scale) and dV are written once per tile.
 //   bwd_dq_kernel    dq = scale * accumulator, rounded to the 16-bit type.
+//
+// Warp roles of bwd_kv_kernel (16 warps, registers re-split with setmaxnreg):
+//   warps 0-3, 4-7   dS warpgroups: key row = lane of tensor memory; warpgroup h
+//                    handles query columns 64h .. 64h+63 of the current block
+//   warps 8-11       dQ warpgroup: reads dQ_part, adds it into the accumulator;
+//                    writes dK and dV at the end of a tile
+//   warp 12          TMA producer; warp 13 MMA issuer; warps 14-15 idle
+//
+// At d = 64 the tensor-memory columns hold S^T, dP^T, dV, dK, dQ and P^T side by side,
+// and the next block's S^T / dP^T are issued as soon as the dS warpgroups have read
+// the current ones, so the tensor core computes them while dS is formed.  At d = 128
+// (512 columns are taken by S^T, dP^T, dV, dK) P^T shares the S^T columns and dQ
+// shares the dP^T columns, and the steps run in order.
 #include <cuda_fp16.h>
 
 #include "internal.h"
@@ -31,22 +45,29 @@ namespace {
 
 constexpr int kRows = 128;
 constexpr int kChunkBytes = kRows * 128;
-constexpr int kBwdThreads = 320;   // ds warpgroup (0-3), dQ warpgroup (4-7), producer (8), MMA (9)
+constexpr int kBwdThreads = 512;
+constexpr int kBwdLaunchRegs = 128;
+constexpr int kDsRegs = 192;
+constexpr int kDqRegs = 56;
+constexpr int kCtlRegs = 72;
+static_assert((2 * kDsRegs + kDqRegs + kCtlRegs) * 128 <= kBwdLaunchRegs * kBwdThreads,
+              "register split exceeds the launch");
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct BwdCfg {
   static constexpr int kChunks = D / 64;
   static constexpr int kTileBytes = kRows * D * 2;
+  static constexpr bool kEarly = (D == 64);          // next S^T / dP^T issued before this block's gradients
   static constexpr int kKVBufs = (D == 64) ? 2 : 1;
-  static constexpr int kQBufs = (D == 64) ? 2 : 1;
+  static constexpr int kQBufs = (D == 64) ? 3 : 1;
+  static_assert(!kEarly || kQBufs >= 2, "early issue needs two Q/dO buffers");
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kKVBufs * kTileBytes;
   static constexpr int kOffQ = kOffV + kKVBufs * kTileBytes;
   static constexpr int kOffDO = kOffQ + kQBufs * kTileBytes;
-  static constexpr int kOffPT = kOffDO + kQBufs * kTileBytes;        // 128 x 128 16-bit, K-major SW128
-  static constexpr int kOffDST = kOffPT + 2 * kChunkBytes;           // 128 x 128 16-bit, K-major SW128
-  static constexpr int kOffStats = kOffDST + 2 * kChunkBytes;        // [kQBufs][2][128] float
+  static constexpr int kOffDST = kOffDO + kQBufs * kTileBytes;       // 128 x 128 16-bit, K-major SW128
+  static constexpr int kOffStats = kOffDST + 2 * kChunkBytes;        // [kQBufs][-lse2[128], -D[128]] float
   static constexpr int kOffBar = kOffStats + kQBufs * 2 * kRows * 4;
   // barriers
   static constexpr int kKVFull = 0;                   // [kKVBufs]
@@ -54,7 +75,8 @@ struct BwdCfg {
   static constexpr int kQFull = kKVEmpty + kKVBufs;   // [kQBufs]
   static constexpr int kQEmpty = kQFull + kQBufs;     // [kQBufs]
   static constexpr int kSFull = kQEmpty + kQBufs;
-  static constexpr int kDSFull = kSFull + 1;
+  static constexpr int kSTFree = kSFull + 1;
+  static constexpr int kDSFull = kSTFree + 1;
   static constexpr int kMmaDone = kDSFull + 1;
   static constexpr int kDQFull = kMmaDone + 1;
   static constexpr int kDQFree = kDQFull + 1;
@@ -68,17 +90,10 @@ struct BwdCfg {
   static constexpr uint32_t kTmDPT = 128;
   static constexpr uint32_t kTmDV = 256;
   static constexpr uint32_t kTmDK = 256 + D;
-  static constexpr uint32_t kTmDQ = (D == 64) ? 384 : 0;   // d = 128 reuses the S^T columns
+  static constexpr uint32_t kTmDQ = (D == 64) ? 384 : 128;
+  // P^T (16-bit pairs along the query dimension), query half h
+  __host__ __device__ static constexpr uint32_t tm_pt(int h) { return D == 64 ? 448 + 32 * h : 64 * h; }
 };
-
-__device__ __forceinline__ void decode_kv_tile(int tile, int BH, int nkb, int causal, int& bh, int& kb) {
-  // Causal: key block kb has nkb - kb query blocks; lightest-last order puts kb = 0 first.
-  (void)nkb;
-  (void)causal;
-  const int r = tile / BH;
-  bh = tile - r * BH;
-  kb = r;
-}
 
 // 16-byte unit `u` (8 elements) of row `r` inside a 128-row x 128-byte swizzled block.
 __device__ __forceinline__ uint32_t sw128_offset(int r, int u) {
@@ -89,7 +104,7 @@ template <int D, int DT, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                  const float* __restrict__ lse2, const float* __restrict__ dvec, float* __restrict__ dq_accum,
+                  const float* __restrict__ nlse2, const float* __restrict__ ndvec, float* __restrict__ dq_accum,
                   uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, int BH, int N, int Npad, float scale,
                   float scale_log2, unsigned int* err_word, uint64_t limit_ns) {
   using C = BwdCfg<D>;
@@ -115,7 +130,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(bar(C::kQEmpty + i), 1);
     }
     mbar_init(bar(C::kSFull), 1);
-    mbar_init(bar(C::kDSFull), kRows);
+    mbar_init(bar(C::kSTFree), 2 * kRows);
+    mbar_init(bar(C::kDSFull), 2 * kRows);
     mbar_init(bar(C::kMmaDone), 1);
     mbar_init(bar(C::kDQFull), 1);
     mbar_init(bar(C::kDQFree), kRows);
@@ -125,7 +141,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == 13) {
     tmem_alloc(smem_u32(tmem_holder), 512);
     tmem_relinquish();
   }
@@ -136,9 +152,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const WaitCtl ctl{abort_flag, err_word, limit_ns};
   const WaitCtl drain{nullptr, err_word, limit_ns};
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ TMA producer (whole warp; one lane issues)
-    {
+  if (warp >= 12) {
+    regs_dec<kCtlRegs>();
+    if (warp == 12) {
+      // ---------------------------------------------------------- TMA producer (whole warp; one lane issues)
       if (elect_one()) {
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
@@ -149,11 +166,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++it) {
-        int bh, kb;
-        decode_kv_tile(tile, BH, nb, CAUSAL, bh, kb);
+        const int kb = tile / BH;          // key block: kb = 0 carries the most query blocks (causal)
+        const int bh = tile - kb * BH;
         const int kvb = it % C::kKVBufs;
-        if (it >= C::kKVBufs &&
-            !wait_warp(bar(C::kKVEmpty + kvb), ((it / C::kKVBufs) - 1) & 1, ctl, 0x401)) {
+        if (it >= C::kKVBufs && !wait_warp(bar(C::kKVEmpty + kvb), ((it / C::kKVBufs) - 1) & 1, ctl, 0x401)) {
           ok = false;
           break;
         }
@@ -171,8 +187,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int q0 = CAUSAL ? kb : 0;
         for (int qi = q0; qi < nb; ++qi, ++s) {
           const int qs = s % C::kQBufs;
-          if (s >= (uint32_t)C::kQBufs &&
-              !wait_warp(bar(C::kQEmpty + qs), ((s / C::kQBufs) - 1) & 1, ctl, 0x402)) {
+          if (s >= (uint32_t)C::kQBufs && !wait_warp(bar(C::kQEmpty + qs), ((s / C::kQBufs) - 1) & 1, ctl, 0x402)) {
             ok = false;
             break;
           }
@@ -187,8 +202,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               tma_load_3d(odst + c * kChunkBytes, &tm_do, bar(C::kQFull + qs), c * 64, qi * kRows, bh);
             }
             const size_t srow = (size_t)bh * Npad + (size_t)qi * kRows;
-            bulk_load(stats, lse2 + srow, kRows * 4, bar(C::kQFull + qs));
-            bulk_load(stats + kRows * 4, dvec + srow, kRows * 4, bar(C::kQFull + qs));
+            bulk_load(stats, nlse2 + srow, kRows * 4, bar(C::kQFull + qs));
+            bulk_load(stats + kRows * 4, ndvec + srow, kRows * 4, bar(C::kQFull + qs));
           }
           __syncwarp();
         }
@@ -206,93 +221,131 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_wait(bar(C::kQFull + b), (last / C::kQBufs) & 1, drain, 0x4f2);
           }
       }
-    }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer (whole warp; one lane issues)
-    {
+    } else if (warp == 13) {
+      // ---------------------------------------------------------- MMA issuer (whole warp; one lane issues)
       constexpr uint32_t ab = (DT == 0) ? 1u : 0u;
       constexpr uint32_t idesc_s = idesc_f16(ab, 0, 0, 128, 128);    // A, B K-major
       constexpr uint32_t idesc_kv = idesc_f16(ab, 0, 1, 128, D);     // A K-major, B MN-major
       constexpr uint32_t idesc_q = idesc_f16(ab, 1, 1, 128, D);      // A MN-major, B MN-major
-      const uint32_t pt = smem_u32(smem + C::kOffPT);
       const uint32_t dst = smem_u32(smem + C::kOffDST);
+      auto qaddr = [&](uint32_t step) { return smem_u32(smem + C::kOffQ + (step % C::kQBufs) * C::kTileBytes); };
+      auto oaddr = [&](uint32_t step) { return smem_u32(smem + C::kOffDO + (step % C::kQBufs) * C::kTileBytes); };
+      // S^T = K Q^T and / or dP^T = V dO^T (A, B K-major, 16 elements = 32 bytes per step)
+      auto issue_st = [&](uint32_t kbase, uint32_t qbase) {
+        const uint64_t kd = sdesc_sw128(kbase, 16, 1024), qd = sdesc_sw128(qbase, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
+          umma_ss(tmem + C::kTmST, kd + off, qd + off, idesc_s, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_dpt = [&](uint32_t vbase, uint32_t obase) {
+        const uint64_t vd = sdesc_sw128(vbase, 16, 1024), od = sdesc_sw128(obase, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
+          umma_ss(tmem + C::kTmDPT, vd + off, od + off, idesc_s, kk > 0 ? 1u : 0u);
+        }
+      };
       uint32_t s = 0;
       int it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++it) {
-        int bh, kb;
-        decode_kv_tile(tile, BH, nb, CAUSAL, bh, kb);
+        const int kb = tile / BH;
         const int kvb = it % C::kKVBufs;
+        const int q0 = CAUSAL ? kb : 0;
+        const int nsteps = nb - q0;
         if (!wait_warp(bar(C::kKVFull + kvb), (it / C::kKVBufs) & 1, ctl, 0x501)) break;
         const uint32_t kbase = smem_u32(smem + C::kOffK + kvb * C::kTileBytes);
         const uint32_t vbase = smem_u32(smem + C::kOffV + kvb * C::kTileBytes);
-        const int q0 = CAUSAL ? kb : 0;
-        for (int qi = q0; qi < nb; ++qi, ++s) {
-          const int qs = s % C::kQBufs;
-          if (!wait_warp(bar(C::kQFull + qs), (s / C::kQBufs) & 1, ctl, 0x502)) {
-            ok = false;
-            break;
+        // first block of the tile
+        if (!wait_warp(bar(C::kQFull + s % C::kQBufs), (s / C::kQBufs) & 1, ctl, 0x502) ||
+            (s > 0 && !wait_warp(bar(C::kSTFree), (s - 1) & 1, ctl, 0x503)) ||
+            (!C::kEarly && s > 0 && !wait_warp(bar(C::kDQFree), (s - 1) & 1, ctl, 0x504))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (elect_one()) {
+          issue_st(kbase, qaddr(s));
+          issue_dpt(vbase, oaddr(s));
+          umma_commit(bar(C::kSFull));
+        }
+        __syncwarp();
+        for (int i = 0; i < nsteps; ++i, ++s) {
+          const bool last = (i == nsteps - 1);
+          if (C::kEarly && !last) {
+            if (!wait_warp(bar(C::kQFull + (s + 1) % C::kQBufs), ((s + 1) / C::kQBufs) & 1, ctl, 0x505) ||
+                !wait_warp(bar(C::kSTFree), s & 1, ctl, 0x506)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            if (elect_one()) {
+              issue_st(kbase, qaddr(s + 1));
+              issue_dpt(vbase, oaddr(s + 1));
+              umma_commit(bar(C::kSFull));
+            }
+            __syncwarp();
           }
-          // the dQ columns (and, at d = 128, the S^T columns they share) must be drained
-          if (s > 0 && !wait_warp(bar(C::kDQFree), (s - 1) & 1, ctl, 0x503)) {
+          if (!wait_warp(bar(C::kDSFull), s & 1, ctl, 0x507) ||
+              (i == 0 && it > 0 && !wait_warp(bar(C::kDKVEmpty), (it - 1) & 1, ctl, 0x508)) ||
+              (C::kEarly && s > 0 && !wait_warp(bar(C::kDQFree), (s - 1) & 1, ctl, 0x509))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t qbase = smem_u32(smem + C::kOffQ + qs * C::kTileBytes);
-          const uint32_t obase = smem_u32(smem + C::kOffDO + qs * C::kTileBytes);
           if (elect_one()) {
-            const uint64_t kd = sdesc_sw128(kbase, 16, 1024), qd = sdesc_sw128(qbase, 16, 1024);
-            const uint64_t vd = sdesc_sw128(vbase, 16, 1024), od = sdesc_sw128(obase, 16, 1024);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-              umma_ss(tmem + C::kTmST, kd + off, qd + off, idesc_s, kk > 0 ? 1u : 0u);
-            }
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-              umma_ss(tmem + C::kTmDPT, vd + off, od + off, idesc_s, kk > 0 ? 1u : 0u);
-            }
-            umma_commit(bar(C::kSFull));
-          }
-          __syncwarp();
-          if (!wait_warp(bar(C::kDSFull), s & 1, ctl, 0x504)) {
-            ok = false;
-            break;
-          }
-          if (qi == q0 && it > 0 && !wait_warp(bar(C::kDKVEmpty), (it - 1) & 1, ctl, 0x505)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t first = (qi == q0) ? 1u : 0u;
-          if (elect_one()) {
-            const uint64_t ptk = sdesc_sw128(pt, 16, 1024), dsk = sdesc_sw128(dst, 16, 1024);
-            const uint64_t omn = sdesc_sw128(obase, kChunkBytes, 1024), qmn = sdesc_sw128(qbase, kChunkBytes, 1024);
-            const uint64_t dsmn = sdesc_sw128(dst, kChunkBytes, 1024), kmn = sdesc_sw128(kbase, kChunkBytes, 1024);
+            const uint32_t qbase = qaddr(s), obase = oaddr(s);
+            const uint64_t dsk = sdesc_sw128(dst, 16, 1024);                 // dS^T, K-major (A of dK)
+            const uint64_t dsmn = sdesc_sw128(dst, kChunkBytes, 1024);       // dS, MN-major (A of dQ)
+            const uint64_t omn = sdesc_sw128(obase, kChunkBytes, 1024);      // dO, MN-major (B of dV)
+            const uint64_t qmn = sdesc_sw128(qbase, kChunkBytes, 1024);      // Q, MN-major (B of dK)
+            const uint64_t kmn = sdesc_sw128(kbase, kChunkBytes, 1024);      // K, MN-major (B of dQ)
 #pragma unroll
             for (int kk = 0; kk < kRows / 16; ++kk) {
-              // A = P^T / dS^T (keys x q, q contiguous): K-major, 16 q = 32 bytes
+              const uint32_t acc = (i == 0 && kk == 0) ? 0u : 1u;
+              const uint32_t rows16 = (kk * 16 * 128) >> 4;                  // 16 rows of 128 bytes
+              // dV += P^T dO: A = P^T from tensor memory (16 query columns = 8 packed columns)
+              umma_ts(tmem + C::kTmDV, tmem + C::tm_pt(kk >> 2) + (kk & 3) * 8, omn + rows16, idesc_kv, acc);
+              // dK += dS^T Q: A = dS^T (keys x q, q contiguous), K-major, 16 q = 32 bytes
               const uint32_t aoff = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-              // B = dO / Q (q x d, d contiguous): MN-major, 16 q = 16 rows of 128 bytes
-              const uint32_t boff = (kk * 16 * 128) >> 4;
-              const uint32_t acc = (first && kk == 0) ? 0u : 1u;
-              umma_ss(tmem + C::kTmDV, ptk + aoff, omn + boff, idesc_kv, acc);
-              umma_ss(tmem + C::kTmDK, dsk + aoff, qmn + boff, idesc_kv, acc);
+              umma_ss(tmem + C::kTmDK, dsk + aoff, qmn + rows16, idesc_kv, acc);
             }
 #pragma unroll
             for (int kk = 0; kk < kRows / 16; ++kk) {
-              // A = dS (q x keys) read from the dS^T block: MN-major, 16 keys = 16 rows
-              // B = K (keys x d, d contiguous): MN-major, 16 keys = 16 rows
-              const uint32_t off = (kk * 16 * 128) >> 4;
-              umma_ss(tmem + C::kTmDQ, dsmn + off, kmn + off, idesc_q, kk > 0 ? 1u : 0u);
+              // dQ = dS K: A = dS (q x keys) read MN-major from the dS^T block; B = K MN-major
+              const uint32_t rows16 = (kk * 16 * 128) >> 4;
+              umma_ss(tmem + C::kTmDQ, dsmn + rows16, kmn + rows16, idesc_q, kk > 0 ? 1u : 0u);
             }
             umma_commit(bar(C::kMmaDone));
-            umma_commit(bar(C::kQEmpty + qs));
+            umma_commit(bar(C::kQEmpty + s % C::kQBufs));
             umma_commit(bar(C::kDQFull));
           }
           __syncwarp();
+          if (!C::kEarly && !last) {
+            // S^T(next) overwrites the S^T columns that P^T(this) shared; tcgen05.mma
+            // from one thread run in issue order, so dV above has read P^T first.
+            if (!wait_warp(bar(C::kQFull + (s + 1) % C::kQBufs), ((s + 1) / C::kQBufs) & 1, ctl, 0x50a) ||
+                !wait_warp(bar(C::kSTFree), s & 1, ctl, 0x50b)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            if (elect_one()) issue_st(kbase, qaddr(s + 1));
+            __syncwarp();
+            // dP^T(next) overwrites the dP^T columns that dQ(this) occupies
+            if (!wait_warp(bar(C::kDQFree), s & 1, ctl, 0x50c)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            if (elect_one()) {
+              issue_dpt(vbase, oaddr(s + 1));
+              umma_commit(bar(C::kSFull));
+            }
+            __syncwarp();
+          }
         }
         if (!ok) break;
         if (elect_one()) {
@@ -305,66 +358,83 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       __syncwarp();
       mbar_wait(bar(C::kDrain), 0, drain, 0x5f1);
     }
-  } else if (warp < 4) {
-    // ------------------------------------------------------------ dS warpgroup (one key row per thread)
-    const int t = threadIdx.x;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    uint8_t* pt = smem + C::kOffPT;
-    uint8_t* dst = smem + C::kOffDST;
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ dS warpgroups
+    regs_inc<kDsRegs>();
+    const int h = warp >> 2;                     // query half
+    const int t = threadIdx.x & 127;             // key row inside the block
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t st_addr = tmem + lane_base + C::kTmST + 64 * h;
+    const uint32_t dpt_addr = tmem + lane_base + C::kTmDPT + 64 * h;
+    const uint32_t pt_addr = tmem + lane_base + C::tm_pt(h);
+    uint8_t* dst_chunk = smem + C::kOffDST + h * kChunkBytes;
+    const uint64_t c2 = f2_pack(scale_log2, scale_log2);
     uint32_t s = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-      int bh, kb;
-      decode_kv_tile(tile, BH, nb, CAUSAL, bh, kb);
-      const int key = kb * kRows + t;
+      const int kb = tile / BH;
       const int q0 = CAUSAL ? kb : 0;
       bool ok = true;
       for (int qi = q0; qi < nb; ++qi, ++s) {
         const int qs = s % C::kQBufs;
         bool w = mbar_wait(bar(C::kSFull), s & 1, ctl, 0x601);
         w = w && mbar_wait(bar(C::kQFull + qs), (s / C::kQBufs) & 1, ctl, 0x602);
-        w = w && (s == 0 || mbar_wait(bar(C::kMmaDone), (s - 1) & 1, ctl, 0x603));
         if (!__all_sync(0xffffffffu, w)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const float* st_lse2 = reinterpret_cast<const float*>(smem + C::kOffStats + qs * 2 * kRows * 4);
-        const float* st_d = st_lse2 + kRows;
+        uint32_t sr[64], pr[64];
+        tmem_ld32(st_addr, sr);
+        tmem_ld32(st_addr + 32, sr + 32);
+        tmem_ld32(dpt_addr, pr);
+        tmem_ld32(dpt_addr + 32, pr + 32);
+        tmem_ld_wait();
+        reg_fence<64>(sr);
+        reg_fence<64>(pr);
+        tc_fence_before();
+        mbar_arrive(bar(C::kSTFree));
+        const float4* nl4 = reinterpret_cast<const float4*>(smem + C::kOffStats + qs * 2 * kRows * 4) + 16 * h;
+        const float4* nd4 = nl4 + 32;
         const bool diag = CAUSAL && (qi == kb);
+        uint32_t pw[32], dw[32];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {   // 16 query columns per chunk
-          uint32_t sr[16], pr[16];
-          tmem_ld16(tmem + lane_base + C::kTmST + c * 16, sr);
-          tmem_ld16(tmem + lane_base + C::kTmDPT + c * 16, pr);
-          tmem_ld_wait();
-          reg_fence<16>(sr);
-          reg_fence<16>(pr);
-          uint32_t pw[8], dw[8];
+        for (int k = 0; k < 16; ++k) {   // 4 query columns per step
+          const float4 L = nl4[k];
+          const float4 Dn = nd4[k];
 #pragma unroll
-          for (int e = 0; e < 16; e += 2) {
-            float p2[2], d2[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int col = c * 16 + e + h;
-              float p = ex2_approx(fmaf(__uint_as_float(sr[e + h]), scale_log2, -st_lse2[col]));
-              if (diag && (qi * kRows + col) < key) p = 0.f;
-              p2[h] = p;
-              d2[h] = p * (__uint_as_float(pr[e + h]) - st_d[col]);
+          for (int hp = 0; hp < 2; ++hp) {
+            const int e = 4 * k + 2 * hp;          // column inside this half
+            float x0, x1;
+            f2_unpack(ffma2(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2,
+                            hp ? f2_pack(L.z, L.w) : f2_pack(L.x, L.y)),
+                      x0, x1);
+            float p0 = ex2_approx(x0);
+            float p1 = ex2_approx(x1);
+            if (diag) {   // key t is visible to query column c iff t <= c
+              if (64 * h + e < t) p0 = 0.f;
+              if (64 * h + e + 1 < t) p1 = 0.f;
             }
-            pw[e >> 1] = pack2<DT>(p2[0], p2[1]);
-            dw[e >> 1] = pack2<DT>(d2[0], d2[1]);
+            const uint64_t pp = f2_pack(p0, p1);
+            const uint64_t dd = fadd2(f2_pack(__uint_as_float(pr[e]), __uint_as_float(pr[e + 1])),
+                                      hp ? f2_pack(Dn.z, Dn.w) : f2_pack(Dn.x, Dn.y));
+            float d0, d1;
+            f2_unpack(fmul2(pp, dd), d0, d1);
+            pw[e >> 1] = pack2<DT>(p0, p1);
+            dw[e >> 1] = pack2<DT>(d0, d1);
           }
-          // columns c*16 .. c*16+15 = 16-byte units 2c, 2c+1 of chunk (c / 4)
-          const int chunk = c >> 2;
-          const int u0 = (c & 3) * 2;
-          uint8_t* prow = pt + chunk * kChunkBytes;
-          uint8_t* drow = dst + chunk * kChunkBytes;
-          *reinterpret_cast<uint4*>(prow + sw128_offset(t, u0)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-          *reinterpret_cast<uint4*>(prow + sw128_offset(t, u0 + 1)) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
-          *reinterpret_cast<uint4*>(drow + sw128_offset(t, u0)) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
-          *reinterpret_cast<uint4*>(drow + sw128_offset(t, u0 + 1)) = make_uint4(dw[4], dw[5], dw[6], dw[7]);
         }
+        // the previous block's gradient MMAs must be done with P^T and dS^T
+        if (!__all_sync(0xffffffffu, s == 0 || mbar_wait(bar(C::kMmaDone), (s - 1) & 1, ctl, 0x603))) {
+          ok = false;
+          break;
+        }
+        tmem_st32(pt_addr, pw);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(dst_chunk + sw128_offset(t, u)) =
+              make_uint4(dw[4 * u], dw[4 * u + 1], dw[4 * u + 2], dw[4 * u + 3]);
         fence_proxy_async_smem();
+        tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar(C::kDSFull));
       }
@@ -372,40 +442,45 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ dQ warpgroup: dQ reduction, dK/dV epilogue
-    const int u = threadIdx.x - 128;
+    regs_dec<kDqRegs>();
+    const int u = threadIdx.x - 256;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t s = 0;
     int it = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
-      int bh, kb;
-      decode_kv_tile(tile, BH, nb, CAUSAL, bh, kb);
+      const int kb = tile / BH;
+      const int bh = tile - kb * BH;
       const int q0 = CAUSAL ? kb : 0;
       bool ok = true;
       for (int qi = q0; qi < nb; ++qi, ++s) {
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kDQFull), s & 1, ctl, 0x701))) {
+        if (!wait_warp(bar(C::kDQFull), s & 1, ctl, 0x701)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        uint32_t r[D];
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) tmem_ld32(tmem + lane_base + C::kTmDQ + c * 32, r + c * 32);
-        tmem_ld_wait();
-        reg_fence<D>(r);
-        tc_fence_before();
-        mbar_arrive(bar(C::kDQFree));
         const int q = qi * kRows + u;
-        if (q < N) {
-          float* dst_row = dq_accum + ((size_t)bh * N + q) * D;
+        float* dst_row = dq_accum + ((size_t)bh * N + q) * D;
 #pragma unroll
-          for (int i = 0; i < D; i += 4)
-            red_add_v4(dst_row + i, __uint_as_float(r[i]), __uint_as_float(r[i + 1]), __uint_as_float(r[i + 2]),
-                       __uint_as_float(r[i + 3]));
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_base + C::kTmDQ + c * 32, r);
+          tmem_ld_wait();
+          reg_fence<32>(r);
+          if (c == D / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(bar(C::kDQFree));
+          }
+          if (q < N) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+              red_add_v4(dst_row + c * 32 + i, __uint_as_float(r[i]), __uint_as_float(r[i + 1]),
+                         __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+          }
         }
       }
       if (!ok) break;
       // dK, dV of this key block
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kDKVFull), it & 1, ctl, 0x702))) break;
+      if (!wait_warp(bar(C::kDKVFull), it & 1, ctl, 0x702)) break;
       tc_fence_after();
       const int key = kb * kRows + u;
 #pragma unroll
@@ -437,19 +512,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
 }
 
-// D = rowsum(dO o O) and lse2 = lse*log2(e) per row, padded rows -> (0, +inf);
-// also zeroes the float32 dQ accumulator.  8 threads per row for d = 64 (16 for
-// d = 128), each reading 16 bytes of O and of dO.
+// -D = -rowsum(dO o O) and -lse*log2(e) per row; padded rows -> (0, -inf).  Also
+// zeroes the float32 dQ accumulator.  8 threads per row for d = 64 (16 for d = 128),
+// each reading 16 bytes of O and of dO.
 template <int D, int DT>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
-                                                      const float* __restrict__ lse, float* __restrict__ dvec,
-                                                      float* __restrict__ lse2, float* __restrict__ dq_accum, int BH,
+                                                      const float* __restrict__ lse, float* __restrict__ ndvec,
+                                                      float* __restrict__ nlse2, float* __restrict__ dq_accum, int BH,
                                                       int N, int Npad, size_t accum_elems) {
   constexpr int kTPR = D / 8;   // threads per row
   const long long gtid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -477,8 +552,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
 #pragma unroll
   for (int off = kTPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (part == 0 && row < rows) {
-    dvec[row] = valid ? acc : 0.f;
-    lse2[row] = valid ? lse[(size_t)bh * N + n] * kLog2e : INFINITY;
+    ndvec[row] = valid ? -acc : 0.f;
+    nlse2[row] = valid ? -lse[(size_t)bh * N + n] * kLog2e : -INFINITY;
   }
   // zero the accumulator (grid-stride, 16 bytes per thread per step)
   const size_t n4 = accum_elems / 4;
@@ -522,6 +597,11 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int stages) {
     auto kern = bwd_kv_kernel<D, DT, CAUSAL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
+    // the setmaxnreg split inside the kernel must fit what the launch provides
+    cudaFuncAttributes attr;
+    e = cudaFuncGetAttributes(&attr, kern);
+    if (e != cudaSuccess) return e;
+    if (attr.numRegs * kBwdThreads < (2 * kDsRegs + kDqRegs + kCtlRegs) * 128) return cudaErrorInvalidConfiguration;
     const int nb = (a.N + kRows - 1) / kRows;
     const int ntiles = a.BH * nb;
     const int grid = ntiles < a.num_sms ? ntiles : a.num_sms;

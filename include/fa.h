@@ -123,9 +123,10 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
  * The three stages fa_bwd runs, one launch each, for callers that want to time or
  * schedule them separately.  Arguments, validation and errors are exactly fa_bwd's;
  * calling the three in this order on one stream with one workspace is fa_bwd.
- *   fa_bwd_preprocess : D_i = sum_c dO_ic O_ic and lse in base 2 into the workspace
- *                       (padding rows of the last block get D = 0, lse = +inf), and
- *                       zeroes the workspace's float32 dQ accumulator.
+ *   fa_bwd_preprocess : -D_i = -sum_c dO_ic O_ic and -lse*log2(e) into the workspace
+ *                       (padding rows of the last block get 0 and -inf, so their
+ *                       probabilities are exactly 0), and zeroes the workspace's
+ *                       float32 dQ accumulator.
  *   fa_bwd_dkdv       : the key/value-outer kernel: writes dk and dv, adds the dQ
  *                       partial products into the accumulator.
  *   fa_bwd_dq_convert : dq = scale * accumulator, rounded to `dtype`.
