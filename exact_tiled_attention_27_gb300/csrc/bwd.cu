@@ -19,15 +19,18 @@
 //                                        (one thread per key row and query half)
 //                      dV += P^T dO      (P^T read from tensor memory)
 //                      dK += dS^T Q, dQ_part = dS K      (dS^T from shared memory)
-//                    dQ_part is added into the float32 accumulator with vector
+//                    dQ_part is added into the float32 accumulator by bulk tensor
 //                    reductions; dK (times scale) and dV are written once per tile.
 //   bwd_dq_kernel    dq = scale * accumulator, rounded to the 16-bit type.
 //
 // Warp roles of bwd_kv_kernel (16 warps, registers re-split with setmaxnreg):
 //   warps 0-3, 4-7   dS warpgroups: key row = lane of tensor memory; warpgroup h
 //                    handles query columns 64h .. 64h+63 of the current block
-//   warps 8-11       dQ warpgroup: reads dQ_part, adds it into the accumulator;
-//                    writes dK and dV at the end of a tile
+//   warps 8-11       dQ warpgroup: copies dQ_part from tensor memory into a swizzled
+//                    shared-memory tile that one thread adds into the float32
+//                    accumulator with a bulk tensor reduction (whole 128-byte
+//                    lines, done by the copy engine); writes dK and dV at the end
+//                    of a tile
 //   warp 12          TMA producer; warp 13 MMA issuer; warps 14-15 idle
 //
 // At d = 64 the tensor-memory columns hold S^T, dP^T, dV, dK, dQ and P^T side by side,
@@ -47,9 +50,9 @@ constexpr int kRows = 128;
 constexpr int kChunkBytes = kRows * 128;
 constexpr int kBwdThreads = 512;
 constexpr int kBwdLaunchRegs = 128;
-constexpr int kDsRegs = 192;
-constexpr int kDqRegs = 56;
-constexpr int kCtlRegs = 72;
+constexpr int kDsRegs = 160;
+constexpr int kDqRegs = 96;
+constexpr int kCtlRegs = 96;
 static_assert((2 * kDsRegs + kDqRegs + kCtlRegs) * 128 <= kBwdLaunchRegs * kBwdThreads,
               "register split exceeds the launch");
 constexpr float kLog2e = 1.4426950408889634f;
@@ -60,14 +63,15 @@ struct BwdCfg {
   static constexpr int kTileBytes = kRows * D * 2;
   static constexpr bool kEarly = (D == 64);          // next S^T / dP^T issued before this block's gradients
   static constexpr int kKVBufs = (D == 64) ? 2 : 1;
-  static constexpr int kQBufs = (D == 64) ? 3 : 1;
+  static constexpr int kQBufs = (D == 64) ? 2 : 1;
   static_assert(!kEarly || kQBufs >= 2, "early issue needs two Q/dO buffers");
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kKVBufs * kTileBytes;
   static constexpr int kOffQ = kOffV + kKVBufs * kTileBytes;
   static constexpr int kOffDO = kOffQ + kQBufs * kTileBytes;
   static constexpr int kOffDST = kOffDO + kQBufs * kTileBytes;       // 128 x 128 16-bit, K-major SW128
-  static constexpr int kOffStats = kOffDST + 2 * kChunkBytes;        // [kQBufs][-lse2[128], -D[128]] float
+  static constexpr int kOffDQS = kOffDST + 2 * kChunkBytes;          // dQ staging: 2 x (128 rows x 32 float), SW128
+  static constexpr int kOffStats = kOffDQS + 2 * kChunkBytes;        // [kQBufs][-lse2[128], -D[128]] float
   static constexpr int kOffBar = kOffStats + kQBufs * 2 * kRows * 4;
   // barriers
   static constexpr int kKVFull = 0;                   // [kKVBufs]
@@ -104,7 +108,7 @@ template <int D, int DT, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                  const float* __restrict__ nlse2, const float* __restrict__ ndvec, float* __restrict__ dq_accum,
+                  const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ nlse2, const float* __restrict__ ndvec, float* __restrict__ dq_accum,
                   uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, int BH, int N, int Npad, float scale,
                   float scale_log2, unsigned int* err_word, uint64_t limit_ns) {
   using C = BwdCfg<D>;
@@ -458,24 +462,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           break;
         }
         tc_fence_after();
-        const int q = qi * kRows + u;
-        float* dst_row = dq_accum + ((size_t)bh * N + q) * D;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_base + C::kTmDQ + c * 32, r);
-          tmem_ld_wait();
-          reg_fence<32>(r);
-          if (c == D / 32 - 1) {
-            tc_fence_before();
-            mbar_arrive(bar(C::kDQFree));
-          }
-          if (q < N) {
+        for (int half = 0; half < D / 64; ++half) {   // 64 columns per staging round
 #pragma unroll
-            for (int i = 0; i < 32; i += 4)
-              red_add_v4(dst_row + c * 32 + i, __uint_as_float(r[i]), __uint_as_float(r[i + 1]),
-                         __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+          for (int c = 0; c < 2; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_base + C::kTmDQ + half * 64 + c * 32, r);
+            tmem_ld_wait();
+            reg_fence<32>(r);
+            if (half == D / 64 - 1 && c == 1) {
+              tc_fence_before();
+              mbar_arrive(bar(C::kDQFree));
+            }
+            uint8_t* box = smem + C::kOffDQS + c * kChunkBytes;
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              *reinterpret_cast<uint4*>(box + sw128_offset(u, v)) =
+                  make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
           }
+          fence_proxy_async_smem();
+          named_bar_sync(1, 128);
+          if (warp == 8) {
+            if (elect_one()) {
+#pragma unroll
+              for (int c = 0; c < 2; ++c)
+                tma_reduce_add_3d(&tm_dq, smem_u32(smem + C::kOffDQS + c * kChunkBytes), (half * 2 + c) * 32,
+                                  qi * kRows, bh);
+              bulk_commit_group();
+              bulk_wait_read_all();   // the staging tile may be overwritten after this
+            }
+            __syncwarp();
+          }
+          named_bar_sync(1, 128);
         }
       }
       if (!ok) break;
@@ -507,6 +525,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(bar(C::kDKVEmpty));
+    }
+    // every bulk reduction issued by this warpgroup must complete before the CTA exits
+    if (warp == 8) {
+      if (elect_one()) bulk_wait_all();
+      __syncwarp();
     }
   }
 
@@ -605,7 +628,8 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int stages) {
     const int nb = (a.N + kRows - 1) / kRows;
     const int ntiles = a.BH * nb;
     const int grid = ntiles < a.num_sms ? ntiles : a.num_sms;
-    kern<<<grid, kBwdThreads, C::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse2, a.dvec, a.dq_accum,
+    kern<<<grid, kBwdThreads, C::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dq, a.lse2, a.dvec,
+                                                        a.dq_accum,
                                                         static_cast<uint16_t*>(a.dk), static_cast<uint16_t*>(a.dv),
                                                         a.BH, a.N, a.Npad, a.scale, a.scale_log2, a.err_word,
                                                         a.limit_ns);

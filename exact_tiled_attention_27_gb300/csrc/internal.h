@@ -27,6 +27,7 @@ struct FwdArgs {
 
 struct BwdArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;
+  CUtensorMap tm_dq;  // 3-D map {d, N, B*H} over the float32 dQ accumulator, box {32, 128, 1}
   const void* o;
   const void* dO;
   const float* lse;
