@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint32_t s = 0;
       int it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++it) {
+      for (int k = 0, tile = persistent_tile(0); ok && tile < ntiles; tile = persistent_tile(++k), ++it) {
         const int kb = tile / BH;          // key block: kb = 0 carries the most query blocks (causal)
         const int bh = tile - kb * BH;
         const int kvb = it % C::kKVBufs;
@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint32_t s = 0;
       int it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++it) {
+      for (int k = 0, tile = persistent_tile(0); ok && tile < ntiles; tile = persistent_tile(++k), ++it) {
         const int kb = tile / BH;
         const int kvb = it % C::kKVBufs;
         const int q0 = CAUSAL ? kb : 0;
@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint8_t* dst_chunk = smem + C::kOffDST + h * kChunkBytes;
     const uint64_t c2 = f2_pack(scale_log2, scale_log2);
     uint32_t s = 0;
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    for (int k = 0, tile = persistent_tile(0); tile < ntiles; tile = persistent_tile(++k)) {
       const int kb = tile / BH;
       const int q0 = CAUSAL ? kb : 0;
       bool ok = true;
@@ -451,7 +451,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t s = 0;
     int it = 0;
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+    for (int k = 0, tile = persistent_tile(0); tile < ntiles; tile = persistent_tile(++k), ++it) {
       const int kb = tile / BH;
       const int bh = tile - kb * BH;
       const int q0 = CAUSAL ? kb : 0;

@@ -40,6 +40,9 @@
 // skipped on most blocks.
 #include <cuda_fp16.h>
 
+#include <algorithm>
+#include <vector>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -87,20 +90,29 @@ struct FwdCfg {
 };
 
 struct TileInfo {
-  int bh, qb0, n0, n1, nkv;
+  int bh, qb0, qb1, n0, n1, nkv;
 };
 
-// Work tile `tile` -> head, first query block and the key/value block counts of the
-// two sub-tiles (n1 = 0 when the second block lies past the sequence end).
-__device__ __forceinline__ TileInfo decode_tile(int tile, int BH, int nqb, bool causal) {
+// Work tile `tile` -> head, the two query blocks and their key/value block counts
+// (n1 = 0 when there is no second block).  Two pairings of the query blocks:
+//   adjacent  (2p, 2p+1): the two sub-tiles share every key/value block; pairs are
+//             numbered heaviest first under the causal mask.
+//   balanced  (i, nqb-1-i): under the causal mask every pair costs nqb+1 blocks, which
+//             evens out the work when there are only about as many pairs as SMs.
+__device__ __forceinline__ TileInfo decode_tile(int tile, int BH, int nqb, bool causal, bool balanced) {
   const int npairs = (nqb + 1) >> 1;
   TileInfo ti;
-  const int r = tile / BH;   // r = 0: the last (heaviest, causal) pair of every head
+  const int r = tile / BH;
   ti.bh = tile - r * BH;
-  const int p = npairs - 1 - r;
-  ti.qb0 = 2 * p;
+  if (balanced) {
+    ti.qb0 = r;
+    ti.qb1 = nqb - 1 - r;
+  } else {
+    ti.qb0 = 2 * (npairs - 1 - r);   // r = 0: the last (heaviest, causal) pair of every head
+    ti.qb1 = ti.qb0 + 1;
+  }
   ti.n0 = causal ? ti.qb0 + 1 : nqb;
-  ti.n1 = (ti.qb0 + 1 < nqb) ? (causal ? ti.qb0 + 2 : nqb) : 0;
+  ti.n1 = (ti.qb1 < nqb && ti.qb1 != ti.qb0) ? (causal ? ti.qb1 + 1 : nqb) : 0;
   ti.nkv = ti.n0 > ti.n1 ? ti.n0 : ti.n1;
   return ti;
 }
@@ -109,7 +121,7 @@ template <int D, int DT, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, uint16_t* __restrict__ out, float* __restrict__ lse,
-               int BH, int N, float scale_log2, unsigned int* err_word, uint64_t limit_ns) {
+               int BH, int N, float scale_log2, int balanced, unsigned int* err_word, uint64_t limit_ns) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -169,8 +181,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t g = 0;
       int it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++it) {
-        const TileInfo ti = decode_tile(tile, BH, nqb, CAUSAL);
+      for (int k = 0, tile = persistent_tile(0); ok && tile < ntiles; tile = persistent_tile(++k), ++it) {
+        const TileInfo ti = decode_tile(tile, BH, nqb, CAUSAL, balanced != 0);
         const int qbuf = it % C::kQBufs;
         if (it >= C::kQBufs && !wait_warp(bar(C::kQEmpty + qbuf), ((it / C::kQBufs) - 1) & 1, ctl, 0x101)) {
           ok = false;
@@ -183,7 +195,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t qdst = smem_u32(smem + C::kOffQ + (qbuf * 2 + t) * C::kTileBytes);
 #pragma unroll
             for (int c = 0; c < C::kChunks; ++c)
-              tma_load_3d(qdst + c * kChunkBytes, &tm_q, bar(C::kQFull + qbuf), c * 64, (ti.qb0 + t) * kTileRows,
+              tma_load_3d(qdst + c * kChunkBytes, &tm_q, bar(C::kQFull + qbuf), c * 64,
+                          (t == 0 ? ti.qb0 : ti.qb1) * kTileRows,
                           ti.bh);
           }
         }
@@ -248,8 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_ss(tmem + C::tm_s(t), qd + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
         }
       };
-      for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++it) {
-        const TileInfo ti = decode_tile(tile, BH, nqb, CAUSAL);
+      for (int k = 0, tile = persistent_tile(0); ok && tile < ntiles; tile = persistent_tile(++k), ++it) {
+        const TileInfo ti = decode_tile(tile, BH, nqb, CAUSAL, balanced != 0);
         const int n[2] = {ti.n0, ti.n1};
         const int qbuf = it % C::kQBufs;
         const uint32_t qbase0 = smem_u32(smem + C::kOffQ + (qbuf * 2) * C::kTileBytes);
@@ -333,11 +346,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t c2 = f2_pack(scale_log2, scale_log2);
     uint32_t c = 0;   // steps of this sub-tile (S-full / P-full phases)
     uint32_t e = 0;   // epilogues of this sub-tile
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-      const TileInfo ti = decode_tile(tile, BH, nqb, CAUSAL);
+    for (int k = 0, tile = persistent_tile(0); tile < ntiles; tile = persistent_tile(++k)) {
+      const TileInfo ti = decode_tile(tile, BH, nqb, CAUSAL, balanced != 0);
       const int n = t == 0 ? ti.n0 : ti.n1;
       if (n == 0) continue;
-      const int qb = ti.qb0 + t;
+      const int qb = t == 0 ? ti.qb0 : ti.qb1;
       const int row = qb * kTileRows + tid;
       float m = -INFINITY;
       float l = 0.f;
@@ -450,6 +463,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Causal pairing choice: simulate the snake schedule of both pairings over `grid`
+// CTAs and keep the one whose busiest CTA has less work (adjacent on ties, since its
+// sub-tiles share more key/value loads).  With many tiles per CTA both balance well,
+// so the simulation is only run for small launches.
+int choose_balanced_pairing(int BH, int nqb, int grid) {
+  const int npairs = (nqb + 1) / 2;
+  const long long ntiles = (long long)BH * npairs;
+  if (ntiles > 8LL * grid) return 0;
+  long long worst[2] = {0, 0};
+  std::vector<long long> load(grid);
+  for (int mode = 0; mode < 2; ++mode) {
+    std::fill(load.begin(), load.end(), 0);
+    for (long long t = 0; t < ntiles; ++t) {
+      const long long r = t / BH;
+      int qb0, qb1;
+      if (mode) {
+        qb0 = (int)r;
+        qb1 = nqb - 1 - (int)r;
+      } else {
+        qb0 = 2 * (npairs - 1 - (int)r);
+        qb1 = qb0 + 1;
+      }
+      const long long cost = (qb0 + 1) + ((qb1 < nqb && qb1 != qb0) ? qb1 + 1 : 0);
+      const long long round = t / grid, pos = t % grid;
+      load[(round & 1) ? grid - 1 - pos : pos] += cost;
+    }
+    worst[mode] = *std::max_element(load.begin(), load.end());
+  }
+  return worst[1] < worst[0] ? 1 : 0;
+}
+
 template <int D, int DT, bool CAUSAL>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   using C = FwdCfg<D>;
@@ -465,8 +509,9 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   const int nqb = (a.N + kTileRows - 1) / kTileRows;
   const int ntiles = a.BH * ((nqb + 1) / 2);
   const int grid = ntiles < a.num_sms ? ntiles : a.num_sms;
+  const int balanced = CAUSAL ? choose_balanced_pairing(a.BH, nqb, grid) : 0;
   kern<<<grid, kThreads, C::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, static_cast<uint16_t*>(a.o), a.lse,
-                                                   a.BH, a.N, a.scale_log2, a.err_word, a.limit_ns);
+                                                   a.BH, a.N, a.scale_log2, balanced, a.err_word, a.limit_ns);
   return cudaGetLastError();
 }
 

@@ -38,6 +38,15 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
+// Persistent schedule: the k-th work tile of this CTA.  Tiles are numbered heaviest
+// first; rounds alternate direction ("snake"), so the CTA that took the heaviest tile
+// of one round takes the lightest of the next.  Per CTA the index grows with k.
+__device__ __forceinline__ int persistent_tile(int k) {
+  const int G = static_cast<int>(gridDim.x);
+  const int c = static_cast<int>(blockIdx.x);
+  return k * G + ((k & 1) ? (G - 1 - c) : c);
+}
+
 // named barrier among `nthreads` threads (multiple of 32)
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
