@@ -294,8 +294,19 @@ def run_ours(args, w, rank, world, local_rank):
     return result
 
 
+KERNEL_SOURCE = {"fwd_kernel": "fwd.cu", "bwd_kv_kernel": "bwd.cu"}
+
+
+def source_sha256(kernel):
+    import hashlib
+    path = os.path.join(ROOT, "exact_tiled_attention_27_gb300", "csrc", KERNEL_SOURCE[kernel])
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
 def traffic_for(kernel, workload):
-    """DRAM bytes per launch from a committed ncu capture of the current kernel, if any."""
+    """DRAM bytes per launch from a committed ncu capture, or None when there is none or
+    the kernel's source has changed since the counters were taken."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -303,8 +314,10 @@ def traffic_for(kernel, workload):
         with open(p) as f:
             j = json.load(f)
         entry = j.get(f"{kernel}:{workload}")
-        return entry.get("bytes_per_launch") if entry else None
-    except (OSError, ValueError):
+        if not entry or entry.get("source_sha256") != source_sha256(kernel):
+            return None
+        return entry.get("bytes_per_launch")
+    except (OSError, ValueError, KeyError):
         return None
 
 
