@@ -31,8 +31,14 @@
 //    O_t += P_t(j) V(j) and commits both to one barrier, so when the softmax sees
 //    S_t(j+1) the previous P.V has already landed in O_t and O_t can be rescaled
 //    without any further wait;
-//  * tcgen05.mma operations issued by one thread execute in issue order (at d = 128
-//    P_t occupies the first 64 columns of S_t's buffer).
+//  * tcgen05.mma operations issued by one thread execute in issue order (P_t occupies
+//    the first 64 columns of S_t's buffer, and S_t(j+1) is issued after P_t(j).V).
+//
+// O is divided by the sum of the 16-bit P values the P.V product actually used, so
+// each output row is an exact convex combination of V rows with those weights and
+// the rounding of a dominant weight cancels; lse uses the sum of the unrounded P.
+// At d = 64 the tensor core forms that sum (a block of ones as 16 more V columns);
+// at d = 128 the softmax threads add it up.
 //
 // The running maximum is only moved when a new row maximum exceeds it by more than
 // 8 (base-2 units).  Until then P entries may reach 2^8; the result is unchanged
@@ -69,7 +75,13 @@ struct FwdCfg {
   static constexpr int kOffQ = 0;                           // [kQBufs][2 sub-tiles]
   static constexpr int kOffK = kOffQ + kQBufs * 2 * kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  // d = 64: a 128-row block of ones forms 16 extra columns of V, so P.V also yields
+  // the sum of the 16-bit P values (O column 64); d = 128 has no tensor-memory columns
+  // to spare and sums them on the CUDA cores instead.
+  static constexpr bool kOnesCol = (D == 64);
+  static constexpr int kOffOnes = kOffV + kStages * kTileBytes;
+  static constexpr int kOffBar = kOffOnes + (kOnesCol ? kChunkBytes : 0);
+  static constexpr uint32_t kPVN = D + (kOnesCol ? 16 : 0);   // N of the P.V MMA
   // barrier indices
   static constexpr int kQFull = 0;                          // [kQBufs]
   static constexpr int kQEmpty = kQFull + kQBufs;           // [kQBufs]
@@ -85,8 +97,9 @@ struct FwdCfg {
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;   // + alignment slack
   // tensor memory columns (512 allocated)
   __host__ __device__ static constexpr uint32_t tm_s(int t) { return t * 128; }
-  __host__ __device__ static constexpr uint32_t tm_p(int t) { return D == 64 ? 256 + t * 64 : t * 128; }
-  __host__ __device__ static constexpr uint32_t tm_o(int t) { return D == 64 ? 384 + t * 64 : 256 + t * 128; }
+  // P_t occupies the first 64 columns of S_t; O_t (kPVN columns) follows the S buffers
+  __host__ __device__ static constexpr uint32_t tm_p(int t) { return t * 128; }
+  __host__ __device__ static constexpr uint32_t tm_o(int t) { return 256 + t * 128; }
 };
 
 struct TileInfo {
@@ -155,6 +168,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(C::kDrain), 1);
     *abort_flag = 0;
     fence_mbar_init();
+  }
+  if constexpr (C::kOnesCol) {
+    // the block of ones read as V columns 64..127 (only 64..79 are used)
+    const uint32_t one2 = (DT == 1) ? 0x3C003C00u : 0x3F803F80u;
+    uint4* ones = reinterpret_cast<uint4*>(smem + C::kOffOnes);
+    for (int i = threadIdx.x; i < kChunkBytes / 16; i += kThreads) ones[i] = make_uint4(one2, one2, one2, one2);
+    fence_proxy_async_smem();
   }
   if (warp == 9) {
     tmem_alloc(smem_u32(tmem_holder), 512);
@@ -245,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
       constexpr uint32_t ab = (DT == 0) ? 1u : 0u;   // instruction-descriptor code: bf16 = 1, fp16 = 0
       constexpr uint32_t idesc_qk = idesc_f16(ab, 0, 0, 128, 128);
-      constexpr uint32_t idesc_pv = idesc_f16(ab, 0, 1, 128, D);
+      constexpr uint32_t idesc_pv = idesc_f16(ab, 0, 1, 128, C::kPVN);
       uint32_t g = 0;
       int it = 0;
       uint32_t c[2] = {0, 0};   // steps issued per sub-tile (S-full / P-full phases)
@@ -303,7 +323,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             if (elect_one()) {
-              const uint64_t vd = sdesc_sw128(vbase, kChunkBytes, 1024);
+              // V's second 64-column block is the next 16 KB (d = 128) or the block of ones
+              const uint32_t lbo = C::kOnesCol ? smem_u32(smem + C::kOffOnes) - vbase : kChunkBytes;
+              const uint64_t vd = sdesc_sw128(vbase, lbo, 1024);
 #pragma unroll
               for (int kk = 0; kk < kTileRows / 16; ++kk) {
                 // B = V (keys x d), d contiguous: MN-major; 16 keys = 16 rows of 128 bytes
@@ -353,7 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qb = t == 0 ? ti.qb0 : ti.qb1;
       const int row = qb * kTileRows + tid;
       float m = -INFINITY;
-      float l = 0.f;
+      float l = 0.f;    // running sum of P as computed: lse = m + log2(l)
+      float lr = 0.f;   // running sum of P as rounded for the MMA: O = (sum P V) / lr
       bool ok = true;
       for (int j = 0; j < n; ++j, ++c) {
         if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kSFull + t), c & 1, ctl, 0x301))) {
@@ -389,7 +412,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float m_new = (mc > m + kRescaleThreshold) ? mc : m;
         const float alpha = ex2_approx(m - m_new);
         const uint64_t nm2 = f2_pack(-m_new, -m_new);
-        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};    // sum of P as computed (for lse)
+        uint64_t accr[4] = {0ull, 0ull, 0ull, 0ull};   // d = 128: sum of P as rounded for the MMA
         uint32_t pk[64];
 #pragma unroll
         for (int q = 0; q < 64; ++q) {
@@ -399,6 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float p1 = ex2_approx(x1);
           acc[q & 3] = fadd2(acc[q & 3], f2_pack(p0, p1));
           pk[q] = pack2<DT>(p0, p1);
+          if constexpr (!C::kOnesCol) accr[q & 3] = fadd2(accr[q & 3], unpack2_f2<DT>(pk[q]));
         }
         tmem_st32(p_addr, pk);
         tmem_st32(p_addr + 32, pk + 32);
@@ -414,12 +439,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
             tmem_st32(o_addr + q * 32, orr);
           }
+          if constexpr (C::kOnesCol) {   // the P-sum columns follow O
+            uint32_t orr[16];
+            tmem_ld16(o_addr + D, orr);
+            tmem_ld_wait();
+            reg_fence<16>(orr);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+            tmem_st16(o_addr + D, orr);
+          }
         }
         float a0, a1, b0, b1;
         f2_unpack(fadd2(acc[0], acc[1]), a0, a1);
         f2_unpack(fadd2(acc[2], acc[3]), b0, b1);
         const float rowsum = (a0 + a1) + (b0 + b1);
         l = l * alpha + rowsum;
+        if constexpr (!C::kOnesCol) {
+          f2_unpack(fadd2(accr[0], accr[1]), a0, a1);
+          f2_unpack(fadd2(accr[2], accr[3]), b0, b1);
+          lr = lr * alpha + ((a0 + a1) + (b0 + b1));
+        }
         m = m_new;
         tmem_st_wait();
         tc_fence_before();
@@ -430,7 +469,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kOFull + t), e & 1, ctl, 0x303))) break;
       ++e;
       tc_fence_after();
-      const float inv_l = 1.0f / l;
+      if constexpr (C::kOnesCol) {   // the MMA summed the 16-bit P values into O column D
+        uint32_t orr[16];
+        tmem_ld16(o_addr + D, orr);
+        tmem_ld_wait();
+        reg_fence<16>(orr);
+        lr = __uint_as_float(orr[0]);
+      }
+      const float inv_l = 1.0f / lr;
       uint8_t* orow = reinterpret_cast<uint8_t*>(out) + ((size_t)ti.bh * N + row) * (D * 2);
 #pragma unroll
       for (int q = 0; q < D / 32; ++q) {

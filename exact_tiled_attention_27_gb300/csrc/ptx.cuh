@@ -284,6 +284,12 @@ __device__ __forceinline__ float lg2_approx(float x) {
   return y;
 }
 
+__device__ __forceinline__ uint64_t f2_pack_early(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
 // pack two floats into one 32-bit word of two 16-bit values: lo -> bits 0..15
 template <int DT>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
@@ -307,6 +313,17 @@ __device__ __forceinline__ float2 unpack2(uint32_t w) {
     f.y = __uint_as_float(w & 0xFFFF0000u);
   }
   return f;
+}
+
+// the two 16-bit values of a packed word, widened exactly to float (lo, hi)
+template <int DT>
+__device__ __forceinline__ uint64_t unpack2_f2(uint32_t w) {
+  if constexpr (DT == 1) {
+    const float2 f = __half22float2(*reinterpret_cast<__half2*>(&w));
+    return f2_pack_early(f.x, f.y);
+  } else {
+    return f2_pack_early(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+  }
 }
 
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {

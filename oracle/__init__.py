@@ -13,6 +13,8 @@ materialising the score matrix S and the probability matrix P on purpose:
 * ``attn_bwd_ref``  -- the textbook gradient of that definition (the pages say only
   that the backward recomputes S and P from Q, K and the saved statistics; the
   formulas are the derivative of the definition above).
+* ``attn_rows_ref`` -- the same definition for selected query rows of one head, for
+  checks at sequence lengths where whole heads are too costly in float64.
 * ``online_softmax_stats`` / ``online_attention_row`` / ``attn_fwd_tiled_ref`` --
   the streaming (m, l) recurrence, used only to check the oracle's own algebra.
 
@@ -30,4 +32,5 @@ from .attention import (  # noqa: F401
     attn_bwd_ref,
     attn_head_fwd,
     attn_head_bwd,
+    attn_rows_ref,
 )

@@ -28,6 +28,7 @@ from __future__ import annotations
 import numpy as np
 
 __all__ = [
+    "attn_rows_ref",
     "softmax_two_pass",
     "online_softmax_stats",
     "online_attention_row",
@@ -225,6 +226,38 @@ def attn_head_bwd(q, k, v, do, scale, causal, row_block=None):
         dk += scale * (ds.T @ q[r0:r1])
         dvec[r0:r1] = d_i[:, 0]
     return dq, dk, dv, dvec
+
+
+def attn_rows_ref(q_rows, rows, k, v, scale, causal, do_rows=None):
+    """The plain definition for selected query rows of one head.
+
+    q_rows: (R, d) query rows whose positions in the sequence are ``rows``; k, v: the
+    whole head (N, d).  Returns (O_rows, LSE_rows) or, when ``do_rows`` is given,
+    (O_rows, LSE_rows, dQ_rows, D_rows) with D_i = sum_j P_ij dP_ij and
+    dQ_i = scale * sum_j P_ij (dP_ij - D_i) K_j -- the same formulas as
+    ``attn_head_fwd`` / ``attn_head_bwd`` restricted to the given rows (each row of S,
+    P, dP depends only on its own query row).
+    """
+    q = np.asarray(q_rows, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    rows = np.asarray(rows)
+    s = scale * (q @ k.T)
+    if causal:
+        s = np.where(np.arange(k.shape[0])[None, :] > rows[:, None], -np.inf, s)
+    m = np.max(s, axis=1, keepdims=True)
+    e = np.exp(s - m)
+    l = np.sum(e, axis=1, keepdims=True)
+    p = e / l
+    o = p @ v
+    lse = (m + np.log(l))[:, 0]
+    if do_rows is None:
+        return o, lse
+    g = np.asarray(do_rows, dtype=np.float64)
+    dp = g @ v.T
+    d_i = np.sum(p * dp, axis=1, keepdims=True)
+    dq = scale * ((p * (dp - d_i)) @ k)
+    return o, lse, dq, d_i[:, 0]
 
 
 # ----------------------------------------------------------------------------------
