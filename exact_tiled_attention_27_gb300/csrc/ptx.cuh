@@ -82,6 +82,21 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity)
   return ok;
 }
 
+// Same test, but a thread whose phase is not complete may be suspended (up to
+// `hint_ns`) until it completes instead of returning at once, so waiting warps do not
+// take issue slots from the warps doing the work.
+__device__ __forceinline__ uint32_t mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok;
+}
+
 // Shared control block of one CTA: abort flag raised by the first wait that gives up.
 struct WaitCtl {
   volatile int* abort_flag;     // shared memory; nullptr = ignore (used when draining)
@@ -98,8 +113,8 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0u) {
+    if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
+    if ((it & 3u) == 0u) {
       if (ctl.abort_flag != nullptr && *ctl.abort_flag) return false;
       if (globaltimer_ns() - t0 > ctl.limit_ns) {
         if (ctl.abort_flag != nullptr) *ctl.abort_flag = 1;
