@@ -45,6 +45,25 @@ def flops(w, which):
     return f / 2 if w["causal"] else f
 
 
+def reduce_step_times(times, device=None):
+    """Max over ranks of per-rank step times (ms): the job is as slow as its slowest
+    replica.  Works with any initialised process group (nccl on GPUs, gloo on CPU);
+    returns the input unchanged when there is no process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return list(times)
+    t = torch.tensor(list(times), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_throughput(world, flops_per_step, ms_per_step):
+    """Whole-job TFLOP/s of `world` replicas that each do `flops_per_step` per step and
+    take (at most, over ranks) `ms_per_step`."""
+    return world * flops_per_step / (ms_per_step * 1e-3) / 1e12
+
+
 def describe(name, w):
     parts = f"B={w['B']} H={w['H']} N={w['N']} d={w['d']} {w['dtype']} {'causal' if w['causal'] else 'non-causal'}"
     mult = f" inputs x{w['mult']:g}" if w["mult"] != 1.0 else ""
@@ -220,14 +239,12 @@ def run_ours(args, w, rank, world, local_rank):
     t_bwd = sum(t_stage)
     t_step = t_fwd + t_bwd
     if world > 1:
-        t = torch.tensor([t_step, t_fwd, t_bwd], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_step, t_fwd, t_bwd = (float(x) for x in t.tolist())
+        t_step, t_fwd, t_bwd = reduce_step_times([t_step, t_fwd, t_bwd], device=dev)
 
     f_fwd = flops(w, "fwd")
     f_bwd = flops(w, "bwd") if w["backward"] else 0.0
     f_step = f_fwd + f_bwd
-    value = world * f_step / (t_step * 1e-3) / 1e12
+    value = job_throughput(world, f_step, t_step)
     peak_burst, peak_sus, peak_src = measured_peaks()
 
     # ---------------------------------------------------------------- end to end (host buffers)
