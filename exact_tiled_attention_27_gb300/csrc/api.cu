@@ -23,6 +23,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceInfo {
   bool ready = false;
   int num_sms = 0;
+  long long l2_bytes = 0;
   int major = 0;
   unsigned int* err_word = nullptr;
 };
@@ -63,6 +64,7 @@ int get_device(DeviceInfo** out) {
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
     d.num_sms = prop.multiProcessorCount;
+    d.l2_bytes = prop.l2CacheSize;
     d.major = prop.major;
     d.err_word = static_cast<unsigned int*>(p);
     d.ready = true;
@@ -114,7 +116,7 @@ constexpr size_t kAlign = 256;
 size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct WsLayout {
-  size_t dvec_off, lse2_off, acc_off, total;
+  size_t sched_off, dvec_off, lse2_off, acc_off, total;
   int Npad;
 };
 
@@ -122,8 +124,9 @@ WsLayout ws_layout(int B, int H, int N, int d) {
   WsLayout w;
   w.Npad = (N + 127) / 128 * 128;
   const size_t rows = (size_t)B * H * w.Npad;
-  w.dvec_off = 0;
-  w.lse2_off = round_up(rows * 4);
+  w.sched_off = 0;                        // tile counter of the dK/dV kernel
+  w.dvec_off = kAlign;
+  w.lse2_off = w.dvec_off + round_up(rows * 4);
   w.acc_off = w.lse2_off + round_up(rows * 4);
   w.total = w.acc_off + round_up((size_t)B * H * N * d * 4);
   return w;
@@ -218,6 +221,7 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
+  a.tile_counter = reinterpret_cast<unsigned int*>(ws + w.sched_off);
   a.dvec = reinterpret_cast<float*>(ws + w.dvec_off);
   a.lse2 = reinterpret_cast<float*>(ws + w.lse2_off);
   a.dq_accum = reinterpret_cast<float*>(ws + w.acc_off);
@@ -233,6 +237,8 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
   a.err_word = dev->err_word;
   a.limit_ns = kWaitLimitNs;
   a.num_sms = dev->num_sms;
+  // every key block re-reads the head's Q and dO (16-bit) and adds into its float32 dQ
+  a.heads_per_group = heads_per_group(8LL * N * d, dev->l2_bytes, BH);
   return launch_bwd(a, static_cast<cudaStream_t>(stream), stages) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 

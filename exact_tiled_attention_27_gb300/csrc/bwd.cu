@@ -56,6 +56,7 @@ constexpr int kCtlRegs = 96;
 static_assert((2 * kDsRegs + kDqRegs + kCtlRegs) * 128 <= kBwdLaunchRegs * kBwdThreads,
               "register split exceeds the launch");
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kTileSlots = 4;   // tile numbers the producer may publish ahead of the slowest role
 
 template <int D>
 struct BwdCfg {
@@ -72,7 +73,8 @@ struct BwdCfg {
   static constexpr int kOffDST = kOffDO + kQBufs * kTileBytes;       // 128 x 128 16-bit, K-major SW128
   static constexpr int kOffDQS = kOffDST + 2 * kChunkBytes;          // dQ staging: 2 x (128 rows x 32 float), SW128
   static constexpr int kOffStats = kOffDQS + 2 * kChunkBytes;        // [kQBufs][-lse2[128], -D[128]] float
-  static constexpr int kOffBar = kOffStats + kQBufs * 2 * kRows * 4;
+  static constexpr int kOffRing = kOffStats + kQBufs * 2 * kRows * 4;   // int[kTileSlots]
+  static constexpr int kOffBar = kOffRing + kTileSlots * 4;
   // barriers
   static constexpr int kKVFull = 0;                   // [kKVBufs]
   static constexpr int kKVEmpty = kKVFull + kKVBufs;  // [kKVBufs]
@@ -86,7 +88,9 @@ struct BwdCfg {
   static constexpr int kDQFree = kDQFull + 1;
   static constexpr int kDKVFull = kDQFree + 1;
   static constexpr int kDKVEmpty = kDKVFull + 1;
-  static constexpr int kDrain = kDKVEmpty + 1;
+  static constexpr int kTileFull = kDKVEmpty + 1;     // [kTileSlots]
+  static constexpr int kTileEmpty = kTileFull + kTileSlots;   // [kTileSlots]
+  static constexpr int kDrain = kTileEmpty + kTileSlots;
   static constexpr int kNumBars = kDrain + 1;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
   // tensor memory columns (512 allocated)
@@ -109,8 +113,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ nlse2, const float* __restrict__ ndvec, float* __restrict__ dq_accum,
+                  unsigned int* __restrict__ tile_counter,
                   uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, int BH, int N, int Npad, float scale,
-                  float scale_log2, unsigned int* err_word, uint64_t limit_ns) {
+                  float scale_log2, int hg, unsigned int* err_word, uint64_t limit_ns) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned base, derived from the __shared__ array by pointer arithmetic so
@@ -143,6 +148,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar(C::kDQFree), kRows);
     mbar_init(bar(C::kDKVFull), 1);
     mbar_init(bar(C::kDKVEmpty), kRows);
+    for (int i = 0; i < kTileSlots; ++i) {
+      mbar_init(bar(C::kTileFull + i), 1);
+      mbar_init(bar(C::kTileEmpty + i), 13);   // every warp but the producer and the two idle ones
+    }
     mbar_init(bar(C::kDrain), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -158,6 +167,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const WaitCtl ctl{abort_flag, err_word, limit_ns};
   const WaitCtl drain{nullptr, err_word, limit_ns};
 
+  // Work tiles: CTA c starts with tile c; the producer warp claims each further tile
+  // from the global counter (heaviest tiles come first in tile order, so this is list
+  // scheduling by decreasing cost) and publishes it to the other roles through a small
+  // ring in shared memory.  -1 ends the loop.
+  int* tile_ring = reinterpret_cast<int*>(smem + C::kOffRing);
+  auto take_tile = [&](int k, uint32_t site) -> int {
+    const int slot = k % kTileSlots;
+    if (!wait_warp(bar(C::kTileFull + slot), (k / kTileSlots) & 1, ctl, site)) return -1;
+    const int tile = reinterpret_cast<volatile int*>(tile_ring)[slot];
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar(C::kTileEmpty + slot));
+    return tile;
+  };
+
   if (warp >= 12) {
     regs_dec<kCtlRegs>();
     if (warp == 12) {
@@ -171,9 +194,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint32_t s = 0;
       int it = 0;
       bool ok = true;
-      for (int k = 0, tile = persistent_tile(0); ok && tile < ntiles; tile = persistent_tile(++k), ++it) {
-        const int kb = tile / BH;          // key block: kb = 0 carries the most query blocks (causal)
-        const int bh = tile - kb * BH;
+      int next = static_cast<int>(blockIdx.x);
+      for (;; ++it) {
+        const int slot = it % kTileSlots;
+        if (it >= kTileSlots && !wait_warp(bar(C::kTileEmpty + slot), ((it / kTileSlots) - 1) & 1, ctl, 0x403)) {
+          ok = false;
+          break;
+        }
+        const int tile = next < ntiles ? next : -1;
+        if ((threadIdx.x & 31) == 0) {
+          tile_ring[slot] = tile;
+          mbar_arrive(bar(C::kTileFull + slot));   // release: the ring entry is visible with the phase
+        }
+        __syncwarp();
+        if (tile < 0) break;
+        int kb, bh;                        // key block: kb = 0 carries the most query blocks (causal)
+        group_order(tile, BH, nb, hg, kb, bh);
         const int kvb = it % C::kKVBufs;
         if (it >= C::kKVBufs && !wait_warp(bar(C::kKVEmpty + kvb), ((it / C::kKVBufs) - 1) & 1, ctl, 0x401)) {
           ok = false;
@@ -213,6 +249,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           __syncwarp();
         }
+        if (!ok) {
+          ++it;   // this tile's K and V were issued: the drain below must wait for them
+          break;
+        }
+        // claim the next tile only now, when this tile's last loads are issued and its
+        // compute is about to end: the order of claims then follows the order in which
+        // CTAs run out of work (list scheduling), not the order in which they started
+        unsigned int claim = 0;
+        if ((threadIdx.x & 31) == 0) claim = atomicAdd(tile_counter, 1u);
+        next = static_cast<int>(gridDim.x + __shfl_sync(0xffffffffu, claim, 0));
       }
       if (!ok) {
         // let every copy already issued land before the CTA exits
@@ -256,8 +302,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint32_t s = 0;
       int it = 0;
       bool ok = true;
-      for (int k = 0, tile = persistent_tile(0); ok && tile < ntiles; tile = persistent_tile(++k), ++it) {
-        const int kb = tile / BH;
+      for (;; ++it) {
+        const int tile = take_tile(it, 0x50f);
+        if (tile < 0) break;
+        int kb, bh;
+        group_order(tile, BH, nb, hg, kb, bh);
         const int kvb = it % C::kKVBufs;
         const int q0 = CAUSAL ? kb : 0;
         const int nsteps = nb - q0;
@@ -376,8 +425,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint8_t* dst_chunk = smem + C::kOffDST + h * kChunkBytes;
     const uint64_t c2 = f2_pack(scale_log2, scale_log2);
     uint32_t s = 0;
-    for (int k = 0, tile = persistent_tile(0); tile < ntiles; tile = persistent_tile(++k)) {
-      const int kb = tile / BH;
+    for (int k = 0;; ++k) {
+      const int tile = take_tile(k, 0x60f);
+      if (tile < 0) break;
+      int kb, bh;
+      group_order(tile, BH, nb, hg, kb, bh);
       const int q0 = CAUSAL ? kb : 0;
       bool ok = true;
       for (int qi = q0; qi < nb; ++qi, ++s) {
@@ -451,11 +503,47 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     regs_dec<kDqRegs>();
     const int u = threadIdx.x - 256;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    // dK (times scale) and dV of the key block, read out of tensor memory; the columns
+    // are handed back to the MMA warp as soon as the last of them is in registers
+    auto write_dkdv = [&](int it, int kb, int bh) -> bool {
+      if (!wait_warp(bar(C::kDKVFull), it & 1, ctl, 0x702)) return false;
+      tc_fence_after();
+      const int key = kb * kRows + u;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col0 = which == 0 ? C::kTmDV : C::kTmDK;
+        const float mul = which == 0 ? 1.0f : scale;
+        uint8_t* grow = reinterpret_cast<uint8_t*>(which == 0 ? dv : dk) + ((size_t)bh * N + key) * (D * 2);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_base + col0 + c * 32, r);
+          tmem_ld_wait();
+          reg_fence<32>(r);
+          if (which == 1 && c == D / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(bar(C::kDKVEmpty));
+          }
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack2<DT>(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
+          if (key < N) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              st_global_v4(grow + c * 64 + i * 16, w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          }
+        }
+      }
+      return true;
+    };
     uint32_t s = 0;
     int it = 0;
-    for (int k = 0, tile = persistent_tile(0); tile < ntiles; tile = persistent_tile(++k), ++it) {
-      const int kb = tile / BH;
-      const int bh = tile - kb * BH;
+    for (;; ++it) {
+      const int tile = take_tile(it, 0x70f);
+      if (tile < 0) break;
+      int kb, bh;
+      group_order(tile, BH, nb, hg, kb, bh);
       const int q0 = CAUSAL ? kb : 0;
       bool ok = true;
       for (int qi = q0; qi < nb; ++qi, ++s) {
@@ -463,24 +551,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ok = false;
           break;
         }
+        // d = 64: the next tile's first gradient MMAs wait for the dK/dV columns, so
+        // those are read out before the last dQ of the tile (at d = 128 the next
+        // tile's first scores wait for the dQ columns instead, so dQ goes first)
+        if (C::kEarly && qi == nb - 1 && !write_dkdv(it, kb, bh)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
 #pragma unroll
         for (int half = 0; half < D / 64; ++half) {   // 64 columns per staging round
+          uint32_t r[2][32];
+#pragma unroll
+          for (int c = 0; c < 2; ++c) tmem_ld32(tmem + lane_base + C::kTmDQ + half * 64 + c * 32, r[c]);
+          tmem_ld_wait();
+          reg_fence<32>(r[0]);
+          reg_fence<32>(r[1]);
+          if (half == D / 64 - 1) {
+            tc_fence_before();
+            mbar_arrive(bar(C::kDQFree));
+          }
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
-            uint32_t r[32];
-            tmem_ld32(tmem + lane_base + C::kTmDQ + half * 64 + c * 32, r);
-            tmem_ld_wait();
-            reg_fence<32>(r);
-            if (half == D / 64 - 1 && c == 1) {
-              tc_fence_before();
-              mbar_arrive(bar(C::kDQFree));
-            }
             uint8_t* box = smem + C::kOffDQS + c * kChunkBytes;
 #pragma unroll
             for (int v = 0; v < 8; ++v)
               *reinterpret_cast<uint4*>(box + sw128_offset(u, v)) =
-                  make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+                  make_uint4(r[c][4 * v], r[c][4 * v + 1], r[c][4 * v + 2], r[c][4 * v + 3]);
           }
           fence_proxy_async_smem();
           named_bar_sync(1, 128);
@@ -499,34 +596,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
       if (!ok) break;
-      // dK, dV of this key block
-      if (!wait_warp(bar(C::kDKVFull), it & 1, ctl, 0x702)) break;
-      tc_fence_after();
-      const int key = kb * kRows + u;
-#pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t col0 = which == 0 ? C::kTmDV : C::kTmDK;
-        const float mul = which == 0 ? 1.0f : scale;
-        uint8_t* grow = reinterpret_cast<uint8_t*>(which == 0 ? dv : dk) + ((size_t)bh * N + key) * (D * 2);
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_base + col0 + c * 32, r);
-          tmem_ld_wait();
-          reg_fence<32>(r);
-          uint32_t w[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            w[i] = pack2<DT>(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
-          if (key < N) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              st_global_v4(grow + c * 64 + i * 16, w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-          }
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(bar(C::kDKVEmpty));
+      if (!C::kEarly && !write_dkdv(it, kb, bh)) break;
     }
     // every bulk reduction issued by this warpgroup must complete before the CTA exits
     if (warp == 8) {
@@ -549,13 +619,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 template <int D, int DT>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
                                                       const float* __restrict__ lse, float* __restrict__ ndvec,
-                                                      float* __restrict__ nlse2, float* __restrict__ dq_accum, int BH,
-                                                      int N, int Npad, size_t accum_elems) {
+                                                      float* __restrict__ nlse2, float* __restrict__ dq_accum,
+                                                      unsigned int* __restrict__ tile_counter, int BH, int N, int Npad,
+                                                      size_t accum_elems) {
   constexpr int kTPR = D / 8;   // threads per row
   const long long gtid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long row = gtid / kTPR;  // padded row index over BH*Npad
   const int part = (int)(gtid % kTPR);
   const long long rows = (long long)BH * Npad;
+  if (gtid == 0) *tile_counter = 0u;
   const int bh = (int)(row / Npad);
   const int n = (int)(row - (long long)bh * Npad);
   float acc = 0.f;
@@ -613,8 +685,8 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int stages) {
     if (blocks < min_blocks) blocks = min_blocks;
     const size_t accum_elems = (size_t)a.BH * a.N * D;
     bwd_pre_kernel<D, DT><<<(unsigned)blocks, 256, 0, stream>>>(
-        static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dO), a.lse, a.dvec, a.lse2, a.dq_accum, a.BH,
-        a.N, a.Npad, accum_elems);
+        static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dO), a.lse, a.dvec, a.lse2, a.dq_accum,
+        a.tile_counter, a.BH, a.N, a.Npad, accum_elems);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -631,9 +703,10 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int stages) {
     const int ntiles = a.BH * nb;
     const int grid = ntiles < a.num_sms ? ntiles : a.num_sms;
     kern<<<grid, kBwdThreads, C::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dq, a.lse2, a.dvec,
-                                                        a.dq_accum,
+                                                        a.dq_accum, a.tile_counter,
                                                         static_cast<uint16_t*>(a.dk), static_cast<uint16_t*>(a.dv),
-                                                        a.BH, a.N, a.Npad, a.scale, a.scale_log2, a.err_word,
+                                                        a.BH, a.N, a.Npad, a.scale, a.scale_log2,
+                                                        a.heads_per_group, a.err_word,
                                                         a.limit_ns);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -37,12 +37,37 @@ struct BwdArgs {
   float* dvec;        // [B*H*Npad]  D = rowsum(dO o O), 0 on padding rows
   float* lse2;        // [B*H*Npad]  lse * log2(e), +inf on padding rows
   float* dq_accum;    // [B*H*N*d]   float32 dQ partial sums
+  unsigned int* tile_counter;  // tiles handed out beyond the first one per CTA
   int BH, N, Npad, d, dtype, causal;
   float scale, scale_log2;
   unsigned int* err_word;
   uint64_t limit_ns;
   int num_sms;
+  int heads_per_group;           // tile order: see group_order
 };
+
+// Order of the persistent work tiles.  A head (b, h) has `units` tiles, unit 0 the
+// heaviest under the causal mask.  Heads are taken in groups of `hg`; inside a group
+// the order is unit-major, so the CTAs running at any one time share the few heads
+// of one group and the tensors those heads re-read stay in L2.  hg >= BH gives the
+// plain unit-major order over all heads.
+__host__ __device__ __forceinline__ void group_order(int tile, int BH, int units, int hg, int& r, int& bh) {
+  const int per_group = hg * units;
+  const int grp = tile / per_group;
+  const int within = tile - grp * per_group;
+  const int gh = (BH - grp * hg) < hg ? (BH - grp * hg) : hg;
+  r = within / gh;
+  bh = grp * hg + (within - r * gh);
+}
+
+// Heads per group so that `bytes_per_head` of re-read data for one group fits in
+// half of the L2 cache (at least 1, at most BH).
+inline int heads_per_group(long long bytes_per_head, long long l2_bytes, int BH) {
+  long long g = (l2_bytes / 2) / (bytes_per_head > 0 ? bytes_per_head : 1);
+  if (g < 1) g = 1;
+  if (g > BH) g = BH;
+  return static_cast<int>(g);
+}
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 // Backward stages: preprocess (D, lse2, zeroed accumulator), the dK/dV kernel with

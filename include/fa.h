@@ -126,9 +126,11 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
  *   fa_bwd_preprocess : -D_i = -sum_c dO_ic O_ic and -lse*log2(e) into the workspace
  *                       (padding rows of the last block get 0 and -inf, so their
  *                       probabilities are exactly 0), and zeroes the workspace's
- *                       float32 dQ accumulator.
+ *                       float32 dQ accumulator and its tile counter.
  *   fa_bwd_dkdv       : the key/value-outer kernel: writes dk and dv, adds the dQ
- *                       partial products into the accumulator.
+ *                       partial products into the accumulator.  Its CTAs take work
+ *                       tiles from the workspace's tile counter, so each fa_bwd_dkdv
+ *                       needs a fa_bwd_preprocess on the same workspace before it.
  *   fa_bwd_dq_convert : dq = scale * accumulator, rounded to `dtype`.
  */
 int fa_bwd_preprocess(const void* q, const void* k, const void* v, const void* o, const void* dO,
