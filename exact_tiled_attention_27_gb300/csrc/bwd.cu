@@ -166,6 +166,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = *tmem_holder;
   const WaitCtl ctl{abort_flag, err_word, limit_ns};
   const WaitCtl drain{nullptr, err_word, limit_ns};
+  // the set-up above overlapped the previous kernel's tail; global memory only from here.
+  // (This grid does not release its dependents early: a dependent grid launched while
+  // these CTAs run measurably slowed them down.)
+  grid_dep_wait();
 
   // Work tiles: CTA c starts with tile c; the producer warp claims each further tile
   // from the global counter (heaviest tiles come first in tile order, so this is list
@@ -627,6 +631,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
   const long long row = gtid / kTPR;  // padded row index over BH*Npad
   const int part = (int)(gtid % kTPR);
   const long long rows = (long long)BH * Npad;
+  grid_dep_wait();
+  grid_dep_launch();
   if (gtid == 0) *tile_counter = 0u;
   const int bh = (int)(row / Npad);
   const int n = (int)(row - (long long)bh * Npad);
@@ -662,6 +668,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
 template <int DT>
 __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ acc, uint16_t* __restrict__ dq,
                                                      float scale, size_t n8) {
+  grid_dep_wait();
+  grid_dep_launch();
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
     const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
     const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
@@ -684,10 +692,9 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int stages) {
     const long long min_blocks = 4LL * a.num_sms;   // enough blocks to zero the accumulator quickly
     if (blocks < min_blocks) blocks = min_blocks;
     const size_t accum_elems = (size_t)a.BH * a.N * D;
-    bwd_pre_kernel<D, DT><<<(unsigned)blocks, 256, 0, stream>>>(
-        static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dO), a.lse, a.dvec, a.lse2, a.dq_accum,
-        a.tile_counter, a.BH, a.N, a.Npad, accum_elems);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_overlapped(bwd_pre_kernel<D, DT>, (unsigned)blocks, 256, 0, stream,
+                                      static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dO), a.lse,
+                                      a.dvec, a.lse2, a.dq_accum, a.tile_counter, a.BH, a.N, a.Npad, accum_elems);
     if (e != cudaSuccess) return e;
   }
   if (stages & kBwdStageKV) {
@@ -702,13 +709,10 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int stages) {
     const int nb = (a.N + kRows - 1) / kRows;
     const int ntiles = a.BH * nb;
     const int grid = ntiles < a.num_sms ? ntiles : a.num_sms;
-    kern<<<grid, kBwdThreads, C::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dq, a.lse2, a.dvec,
-                                                        a.dq_accum, a.tile_counter,
-                                                        static_cast<uint16_t*>(a.dk), static_cast<uint16_t*>(a.dv),
-                                                        a.BH, a.N, a.Npad, a.scale, a.scale_log2,
-                                                        a.heads_per_group, a.err_word,
-                                                        a.limit_ns);
-    e = cudaGetLastError();
+    e = launch_overlapped(kern, grid, kBwdThreads, C::kSmemBytes, stream, a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dq,
+                          a.lse2, a.dvec, a.dq_accum, a.tile_counter, static_cast<uint16_t*>(a.dk),
+                          static_cast<uint16_t*>(a.dv), a.BH, a.N, a.Npad, a.scale, a.scale_log2,
+                          a.heads_per_group, a.err_word, a.limit_ns);
     if (e != cudaSuccess) return e;
   }
   if (stages & kBwdStageDQ) {
@@ -716,8 +720,8 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int stages) {
     long long blocks = (long long)((n8 + 255) / 256);
     if (blocks > 8LL * a.num_sms) blocks = 8LL * a.num_sms;
     if (blocks < 1) blocks = 1;
-    bwd_dq_kernel<DT><<<(unsigned)blocks, 256, 0, stream>>>(a.dq_accum, static_cast<uint16_t*>(a.dq), a.scale, n8);
-    return cudaGetLastError();
+    return launch_overlapped(bwd_dq_kernel<DT>, (unsigned)blocks, 256, 0, stream, a.dq_accum,
+                             static_cast<uint16_t*>(a.dq), a.scale, n8);
   }
   return cudaSuccess;
 }

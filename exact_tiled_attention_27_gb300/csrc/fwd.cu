@@ -188,6 +188,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_holder;
   const WaitCtl ctl{abort_flag, err_word, limit_ns};
   const WaitCtl drain{nullptr, err_word, limit_ns};
+  // the set-up above overlapped the previous kernel's tail; global memory only from here.
+  // (Dependents are not released early: they start when this grid completes.)
+  grid_dep_wait();
 
   if (warp >= 8) {
     regs_dec<kOtherRegs>();
@@ -558,9 +561,9 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   const int ntiles = a.BH * ((nqb + 1) / 2);
   const int grid = ntiles < a.num_sms ? ntiles : a.num_sms;
   const int balanced = CAUSAL ? choose_balanced_pairing(a.BH, nqb, grid) : 0;
-  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, static_cast<uint16_t*>(a.o), a.lse,
-                                                   a.BH, a.N, a.scale_log2, balanced, a.err_word, a.limit_ns);
-  return cudaGetLastError();
+  return launch_overlapped(kern, grid, kThreads, C::kSmemBytes, stream, a.tm_q, a.tm_k, a.tm_v,
+                           static_cast<uint16_t*>(a.o), a.lse, a.BH, a.N, a.scale_log2, balanced, a.err_word,
+                           a.limit_ns);
 }
 
 }  // namespace

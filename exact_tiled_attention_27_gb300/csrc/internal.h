@@ -69,6 +69,25 @@ inline int heads_per_group(long long bytes_per_head, long long l2_bytes, int BH)
   return static_cast<int>(g);
 }
 
+// Launch with programmatic stream serialization: the kernel may start while the
+// previous kernel in the stream drains; every kernel here calls grid_dep_wait before
+// it reads or writes global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_overlapped(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                              cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 // Backward stages: preprocess (D, lse2, zeroed accumulator), the dK/dV kernel with
 // dQ partial sums, and the dQ conversion.

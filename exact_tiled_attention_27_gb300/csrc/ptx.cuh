@@ -47,6 +47,13 @@ __device__ __forceinline__ int persistent_tile(int k) {
   return k * G + ((k & 1) ? (G - 1 - c) : c);
 }
 
+// Programmatic dependent launch.  grid_dep_wait blocks until the grids this launch
+// depends on have completed and their memory is visible (it returns at once when the
+// launch has no such dependency); grid_dep_launch lets the next launch in the stream
+// start its CTAs as SMs free up (they still wait for this grid before touching memory).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // named barrier among `nthreads` threads (multiple of 32)
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
