@@ -17,6 +17,11 @@ materialising the score matrix S and the probability matrix P on purpose:
   checks at sequence lengths where whole heads are too costly in float64.
 * ``online_softmax_stats`` / ``online_attention_row`` / ``attn_fwd_tiled_ref`` --
   the streaming (m, l) recurrence, used only to check the oracle's own algebra.
+* ``attn_cross_head_fwd`` / ``attn_cross_fwd_ref`` -- the definition with Nq query
+  rows against Nk keys (causal mask aligned bottom-right) and with grouped key/value
+  heads (``kv_head_of``); ``attn_gqa_bwd_ref`` -- its gradient for grouped heads.
+* ``merge_partials`` -- attention over a union of disjoint key ranges from the
+  attention over each range (the split-key combine).
 
 Parity pins: every function here is pinned by tests in ``tests/test_oracle_pins.py``
 against printed worked examples, closed forms, invariants, library routines and
@@ -33,4 +38,9 @@ from .attention import (  # noqa: F401
     attn_head_fwd,
     attn_head_bwd,
     attn_rows_ref,
+    attn_cross_head_fwd,
+    attn_cross_fwd_ref,
+    attn_gqa_bwd_ref,
+    kv_head_of,
+    merge_partials,
 )

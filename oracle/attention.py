@@ -28,6 +28,11 @@ from __future__ import annotations
 import numpy as np
 
 __all__ = [
+    "attn_cross_head_fwd",
+    "attn_cross_fwd_ref",
+    "attn_gqa_bwd_ref",
+    "kv_head_of",
+    "merge_partials",
     "attn_rows_ref",
     "softmax_two_pass",
     "online_softmax_stats",
@@ -338,4 +343,124 @@ def attn_fwd_tiled_ref(q, k, v, scale, causal, block_q, block_k):
             m = m_new
         o[r0:r1] = acc / l[:, None]
         lse[r0:r1] = m + np.log(l)
+    return o, lse
+
+
+# ----------------------------------------------------------------------------------
+# cross lengths (Nq != Nk), grouped key/value heads, split key ranges
+# ----------------------------------------------------------------------------------
+def _cross_scores(q, k, scale, causal):
+    """S = scale * Q K^T for Nq query rows against Nk keys, causal bottom-right.
+
+    With Nq != Nk the pages give no alignment; the reading taken here is the one under
+    which the last query row is the newest token ([FA-practice] §3.1 describes
+    decoding a new token against a key/value cache): key j is visible to query i
+    iff j <= i + (Nk - Nq).  Nq = Nk gives the square mask of ``_scores``.
+    """
+    s = scale * (q @ k.T)
+    if causal:
+        nq, nk = q.shape[0], k.shape[0]
+        rows = np.arange(nq)[:, None] + (nk - nq)
+        cols = np.arange(nk)[None, :]
+        s = np.where(cols > rows, -np.inf, s)
+    return s
+
+
+def attn_cross_head_fwd(q, k, v, scale, causal):
+    """Exact attention of one head with Nq query rows and Nk keys: (O, LSE).
+
+    The definition of ``attn_head_fwd`` with the bottom-right causal mask of
+    ``_cross_scores``.  A row with no visible key (only when causal and Nk < Nq) has
+    an empty softmax; the reading taken is O = 0 and LSE = -inf (the limit of a sum
+    of no terms: l = 0, ln l = -inf).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    s = _cross_scores(q, k, scale, causal)
+    o = np.zeros((q.shape[0], v.shape[1]))
+    lse = np.full(q.shape[0], -np.inf)
+    live = np.isfinite(s).any(axis=1)
+    if live.any():
+        sl = s[live]
+        m = np.max(sl, axis=1, keepdims=True)
+        e = np.exp(sl - m)
+        l = np.sum(e, axis=1, keepdims=True)
+        o[live] = (e / l) @ v
+        lse[live] = (m + np.log(l))[:, 0]
+    return o, lse
+
+
+def kv_head_of(h, H, Hkv):
+    """Key/value head read by query head h when H query heads share Hkv key/value
+    heads (grouped-query attention): consecutive groups of G = H / Hkv query heads
+    share one key/value head, h -> h // G.  The pages name grouped-query attention
+    only as orthogonal to the tiling ("大模型数学速成（17）" §五); the grouping used is
+    the usual contiguous one.  Hkv = H is ordinary multi-head attention.
+    """
+    if H % Hkv:
+        raise ValueError("H must be a multiple of Hkv")
+    return h // (H // Hkv)
+
+
+def attn_cross_fwd_ref(q, k, v, scale, causal, heads=None):
+    """Forward over q (B, H, Nq, d) and k, v (B, Hkv, Nk, d): (O, LSE), float64.
+
+    Query head h reads key/value head ``kv_head_of(h, H, Hkv)``; each (b, h) is
+    ``attn_cross_head_fwd``.  ``heads`` restricts the work to (b, h) pairs (others NaN).
+    """
+    _check4(q, k, v)
+    B, H, Nq, _ = np.shape(q)
+    Hkv = np.shape(k)[1]
+    o = np.full((B, H, Nq, np.shape(v)[3]), np.nan)
+    lse = np.full((B, H, Nq), np.nan)
+    pairs = heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]
+    for b, h in pairs:
+        hk = kv_head_of(h, H, Hkv)
+        o[b, h], lse[b, h] = attn_cross_head_fwd(q[b, h], k[b, hk], v[b, hk], scale, causal)
+    return o, lse
+
+
+def attn_gqa_bwd_ref(q, k, v, do, scale, causal, row_block=None):
+    """Backward with grouped key/value heads, square N: (dQ, dK, dV), float64.
+
+    Every query head h is the ordinary attention of its own Q against key/value head
+    kv_head_of(h); a key/value head's gradient is therefore the sum, over the query
+    heads that read it, of the per-head gradients of ``attn_head_bwd``.
+    """
+    _check4(q, k, v, do)
+    B, H, N, _ = np.shape(q)
+    Hkv = np.shape(k)[1]
+    dq = np.empty(np.shape(q))
+    dk = np.zeros(np.shape(k))
+    dv = np.zeros(np.shape(v))
+    for b in range(B):
+        for h in range(H):
+            hk = kv_head_of(h, H, Hkv)
+            gq, gk, gv, _ = attn_head_bwd(q[b, h], k[b, hk], v[b, hk], do[b, h], scale, causal, row_block)
+            dq[b, h] = gq
+            dk[b, hk] += gk
+            dv[b, hk] += gv
+    return dq, dk, dv
+
+
+def merge_partials(o_parts, lse_parts):
+    """Combine attention over disjoint key ranges into attention over their union.
+
+    Part s holds O_s (rows x d, normalised over its own keys) and LSE_s; the union
+    has LSE = ln sum_s e^{LSE_s} and O = sum_s e^{LSE_s - LSE} O_s.  This is the
+    block-local merge of [FA-review] "方法细节" (l_new = e^{m-m_new} l + e^{m~-m_new} l~)
+    with each part's (m, l) folded into LSE_s = m_s + ln l_s.  Parts with LSE_s = -inf
+    (no visible key) contribute nothing; if every part is empty, O = 0, LSE = -inf.
+    """
+    o_parts = [np.asarray(o, dtype=np.float64) for o in o_parts]
+    lse_parts = np.stack([np.asarray(x, dtype=np.float64) for x in lse_parts])   # (S, rows)
+    m = np.max(lse_parts, axis=0)
+    safe = np.where(np.isneginf(m), 0.0, m)
+    w = np.where(np.isneginf(lse_parts), 0.0, np.exp(lse_parts - safe[None, :]))
+    tot = np.sum(w, axis=0)
+    lse = np.where(tot > 0, safe + np.log(np.where(tot > 0, tot, 1.0)), -np.inf)
+    o = np.zeros_like(o_parts[0])
+    for s_, op in enumerate(o_parts):
+        o += (w[s_] / np.where(tot > 0, tot, 1.0))[:, None] * op
     return o, lse
