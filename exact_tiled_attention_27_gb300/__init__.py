@@ -20,6 +20,7 @@ from .binding import (  # noqa: F401
     debug_wait_timeout,
     device_sm_count,
     forward,
+    forward_cross,
     last_kernel_status,
     load_library,
     strerror,

@@ -49,6 +49,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
         lib.fa_fwd.restype = i
+        lib.fa_fwd_cross.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp]
+        lib.fa_fwd_cross.restype = i
         lib.fa_bwd_workspace_size.argtypes = [i, i, i, i]
         lib.fa_bwd_workspace_size.restype = sz
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, f, i, i, vp]
@@ -144,6 +146,32 @@ def forward(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None):
                                1 if causal else 0, _dtype_code(q), _stream_handle(stream))
     if st != 0:
         raise FaError(st, "fa_fwd")
+    return out, lse
+
+
+def forward_cross(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None):
+    """Forward with Nq != Nk and grouped key/value heads.  q: (B, H, Nq, d); k, v:
+    (B, Hkv, Nk, d) with Hkv dividing H.  The causal mask is aligned bottom-right
+    (query i sees key j iff j <= i + Nk - Nq).  Returns (o, lse) like ``forward``.
+    """
+    torch = _torch()
+    B, H, Nq, d = q.shape
+    Hkv, Nk = int(k.shape[1]), int(k.shape[2])
+    _check_bhnd("q", q, (B, H, Nq, d), q.dtype)
+    _check_bhnd("k", k, (B, Hkv, Nk, d), q.dtype)
+    _check_bhnd("v", v, (B, Hkv, Nk, d), q.dtype)
+    scale = float(d) ** -0.5 if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    _check_bhnd("out", out, (B, H, Nq, d), q.dtype)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, Nq) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 (B, H, Nq) tensor")
+    st = load_library().fa_fwd_cross(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, Nq, Nk, d,
+                                     scale, 1 if causal else 0, _dtype_code(q), _stream_handle(stream))
+    if st != 0:
+        raise FaError(st, "fa_fwd_cross")
     return out, lse
 
 

@@ -160,9 +160,12 @@ using namespace fa;
 
 extern "C" {
 
-int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d, float scale,
-           int causal, int dtype, void* stream) {
-  int st = check_common(B, H, N, d, scale, dtype);
+static int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv,
+                      int Nq, int Nk, int d, float scale, int causal, int dtype, void* stream) {
+  int st = check_common(B, H, Nq, d, scale, dtype);
+  if (st != FA_OK) return st;
+  if (Hkv < 1 || Hkv > H || H % Hkv != 0) return FA_ERR_SHAPE;
+  st = check_common(B, Hkv, Nk, d, scale, dtype);
   if (st != FA_OK) return st;
   if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u))
@@ -172,13 +175,16 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   if (st != FA_OK) return st;
   FwdArgs a;
   const int BH = B * H;
-  if (!encode_bhnd(&a.tm_q, q, BH, N, d, dtype) || !encode_bhnd(&a.tm_k, k, BH, N, d, dtype) ||
-      !encode_bhnd(&a.tm_v, v, BH, N, d, dtype))
+  if (!encode_bhnd(&a.tm_q, q, BH, Nq, d, dtype) || !encode_bhnd(&a.tm_k, k, B * Hkv, Nk, d, dtype) ||
+      !encode_bhnd(&a.tm_v, v, B * Hkv, Nk, d, dtype))
     return FA_ERR_LAUNCH;
   a.o = o;
   a.lse = lse;
   a.BH = BH;
-  a.N = N;
+  a.H = H;
+  a.G = H / Hkv;
+  a.Nq = Nq;
+  a.Nk = Nk;
   a.d = d;
   a.dtype = dtype;
   a.causal = causal ? 1 : 0;
@@ -187,6 +193,16 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   a.limit_ns = kWaitLimitNs;
   a.num_sms = dev->num_sms;
   return launch_fwd(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d, float scale,
+           int causal, int dtype, void* stream) {
+  return fwd_common(q, k, v, o, lse, B, H, H, N, N, d, scale, causal, dtype, stream);
+}
+
+int fa_fwd_cross(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int Nq,
+                 int Nk, int d, float scale, int causal, int dtype, void* stream) {
+  return fwd_common(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, scale, causal, dtype, stream);
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {

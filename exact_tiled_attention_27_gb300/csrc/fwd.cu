@@ -103,8 +103,23 @@ struct FwdCfg {
 };
 
 struct TileInfo {
-  int bh, qb0, qb1, n0, n1, nkv;
+  int bh, kvh, qb0, qb1, n0, n1, nkv;
+  bool has1;   // the second query block exists (it may still see no key)
 };
+
+// Key/value blocks visible to query block qb: all of them without the causal mask;
+// with it, up to the last key the block's last row may see.  The causal mask is
+// aligned bottom-right: key j is visible to query i iff j <= i + (Nk - Nq), which is
+// the square mask when Nq = Nk.  0 when no row of the block sees any key.
+__host__ __device__ __forceinline__ int visible_kv_blocks(int qb, int Nq, int Nk, bool causal) {
+  const int nkb = (Nk + kTileRows - 1) / kTileRows;
+  if (!causal) return nkb;
+  const int last_row = min(Nq - 1, qb * kTileRows + kTileRows - 1);
+  const long long last_key = (long long)last_row + (Nk - Nq);
+  if (last_key < 0) return 0;
+  const int n = (int)(last_key / kTileRows) + 1;
+  return n < nkb ? n : nkb;
+}
 
 // Work tile `tile` -> head, the two query blocks and their key/value block counts
 // (n1 = 0 when there is no second block).  Two pairings of the query blocks:
@@ -112,11 +127,15 @@ struct TileInfo {
 //             numbered heaviest first under the causal mask.
 //   balanced  (i, nqb-1-i): under the causal mask every pair costs nqb+1 blocks, which
 //             evens out the work when there are only about as many pairs as SMs.
-__device__ __forceinline__ TileInfo decode_tile(int tile, int BH, int nqb, bool causal, bool balanced) {
+template <bool GEN>
+__device__ __forceinline__ TileInfo decode_tile(int tile, int BH, int H, int G, int Nq, int Nk, bool causal,
+                                                bool balanced) {
+  const int nqb = (Nq + kTileRows - 1) / kTileRows;
   const int npairs = (nqb + 1) >> 1;
   TileInfo ti;
   const int r = tile / BH;
   ti.bh = tile - r * BH;
+  ti.kvh = GEN ? (ti.bh / H) * (H / G) + (ti.bh % H) / G : ti.bh;
   if (balanced) {
     ti.qb0 = r;
     ti.qb1 = nqb - 1 - r;
@@ -124,17 +143,26 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, int BH, int nqb, bool 
     ti.qb0 = 2 * (npairs - 1 - r);   // r = 0: the last (heaviest, causal) pair of every head
     ti.qb1 = ti.qb0 + 1;
   }
-  ti.n0 = causal ? ti.qb0 + 1 : nqb;
-  ti.n1 = (ti.qb1 < nqb && ti.qb1 != ti.qb0) ? (causal ? ti.qb1 + 1 : nqb) : 0;
+  ti.has1 = ti.qb1 < nqb && ti.qb1 != ti.qb0;
+  if constexpr (GEN) {
+    ti.n0 = visible_kv_blocks(ti.qb0, Nq, Nk, causal);
+    ti.n1 = ti.has1 ? visible_kv_blocks(ti.qb1, Nq, Nk, causal) : 0;
+  } else {   // Nq = Nk: block qb sees blocks 0..qb under the causal mask
+    ti.n0 = causal ? ti.qb0 + 1 : nqb;
+    ti.n1 = ti.has1 ? (causal ? ti.qb1 + 1 : nqb) : 0;
+  }
   ti.nkv = ti.n0 > ti.n1 ? ti.n0 : ti.n1;
   return ti;
 }
 
-template <int D, int DT, bool CAUSAL>
+// GEN: Nq != Nk or grouped key/value heads (fa_fwd_cross); otherwise Nq = Nk and every
+// query head has its own key/value head, and rows always see at least one key.
+template <int D, int DT, bool CAUSAL, bool GEN>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, uint16_t* __restrict__ out, float* __restrict__ lse,
-               int BH, int N, float scale_log2, int balanced, unsigned int* err_word, uint64_t limit_ns) {
+               int BH, int H, int G, int Nq, int Nk, float scale_log2, int balanced, unsigned int* err_word,
+               uint64_t limit_ns) {
   using C = FwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned base, derived from the __shared__ array by pointer arithmetic so
@@ -148,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // warp index through a shuffle so the compiler can treat it (and every TMEM
   // address, descriptor and loop bound derived from it) as warp-uniform
   const int warp = __shfl_sync(0xffffffffu, threadIdx.x >> 5, 0);
-  const int nqb = (N + kTileRows - 1) / kTileRows;
+  const int nqb = (Nq + kTileRows - 1) / kTileRows;
   const int ntiles = BH * ((nqb + 1) >> 1);
 
   if (threadIdx.x == 0) {
@@ -207,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0;
       bool ok = true;
       for (int k = 0, tile = persistent_tile(0); ok && tile < ntiles; tile = persistent_tile(++k), ++it) {
-        const TileInfo ti = decode_tile(tile, BH, nqb, CAUSAL, balanced != 0);
+        const TileInfo ti = decode_tile<GEN>(tile, BH, H, G, Nq, Nk, CAUSAL, balanced != 0);
         const int qbuf = it % C::kQBufs;
         if (it >= C::kQBufs && !wait_warp(bar(C::kQEmpty + qbuf), ((it / C::kQBufs) - 1) & 1, ctl, 0x101)) {
           ok = false;
@@ -239,11 +267,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(bar(C::kKFull + st), C::kTileBytes);
 #pragma unroll
             for (int c = 0; c < C::kChunks; ++c)
-              tma_load_3d(kdst + c * kChunkBytes, &tm_k, bar(C::kKFull + st), c * 64, j * kTileRows, ti.bh);
+              tma_load_3d(kdst + c * kChunkBytes, &tm_k, bar(C::kKFull + st), c * 64, j * kTileRows, ti.kvh);
             mbar_arrive_expect_tx(bar(C::kVFull + st), C::kTileBytes);
 #pragma unroll
             for (int c = 0; c < C::kChunks; ++c)
-              tma_load_3d(vdst + c * kChunkBytes, &tm_v, bar(C::kVFull + st), c * 64, j * kTileRows, ti.bh);
+              tma_load_3d(vdst + c * kChunkBytes, &tm_v, bar(C::kVFull + st), c * 64, j * kTileRows, ti.kvh);
           }
           __syncwarp();
         }
@@ -287,11 +315,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       for (int k = 0, tile = persistent_tile(0); ok && tile < ntiles; tile = persistent_tile(++k), ++it) {
-        const TileInfo ti = decode_tile(tile, BH, nqb, CAUSAL, balanced != 0);
+        const TileInfo ti = decode_tile<GEN>(tile, BH, H, G, Nq, Nk, CAUSAL, balanced != 0);
         const int n[2] = {ti.n0, ti.n1};
         const int qbuf = it % C::kQBufs;
         const uint32_t qbase0 = smem_u32(smem + C::kOffQ + (qbuf * 2) * C::kTileBytes);
         if (!wait_warp(bar(C::kQFull + qbuf), (it / C::kQBufs) & 1, ctl, 0x201)) break;
+        if (GEN && ti.nkv == 0) {   // no query row of the tile sees a key: nothing to multiply
+          if (elect_one()) umma_commit(bar(C::kQEmpty + qbuf));
+          __syncwarp();
+          continue;
+        }
         if (!wait_warp(bar(C::kKFull + g % C::kStages), (g / C::kStages) & 1, ctl, 0x202)) break;
         tc_fence_after();
         {
@@ -374,11 +407,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t c = 0;   // steps of this sub-tile (S-full / P-full phases)
     uint32_t e = 0;   // epilogues of this sub-tile
     for (int k = 0, tile = persistent_tile(0); tile < ntiles; tile = persistent_tile(++k)) {
-      const TileInfo ti = decode_tile(tile, BH, nqb, CAUSAL, balanced != 0);
+      const TileInfo ti = decode_tile<GEN>(tile, BH, H, G, Nq, Nk, CAUSAL, balanced != 0);
       const int n = t == 0 ? ti.n0 : ti.n1;
-      if (n == 0) continue;
       const int qb = t == 0 ? ti.qb0 : ti.qb1;
       const int row = qb * kTileRows + tid;
+      if (n == 0) {
+        // no row of this block sees a key (causal, Nk < Nq): O = 0 and lse = -inf
+        if (GEN && (t == 0 || ti.has1) && row < Nq) {
+          uint8_t* orow = reinterpret_cast<uint8_t*>(out) + ((size_t)ti.bh * Nq + row) * (D * 2);
+#pragma unroll
+          for (int i = 0; i < D / 8; ++i) st_global_v4(orow + i * 16, 0u, 0u, 0u, 0u);
+          lse[(size_t)ti.bh * Nq + row] = -INFINITY;
+        }
+        continue;
+      }
+      // last key visible to this thread's row, and to the block's first row (the same
+      // for the whole warpgroup: key blocks ending past it take the masked path)
+      const int lim_row = CAUSAL ? min(Nk - 1, row + (Nk - Nq)) : (Nk - 1);
+      const int lim_blk = CAUSAL ? min(Nk - 1, qb * kTileRows + (Nk - Nq)) : (Nk - 1);
+      (void)lim_blk;
       float m = -INFINITY;
       float l = 0.f;    // running sum of P as computed: lse = m + log2(l)
       float lr = 0.f;   // running sum of P as rounded for the MMA: O = (sum P V) / lr
@@ -396,11 +443,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         reg_fence<128>(sr);
         float* s = reinterpret_cast<float*>(sr);
         const int kbase = j * kTileRows;
-        if ((kbase + kTileRows > N) || (CAUSAL && j == qb)) {
-          const int lim = CAUSAL ? min(N - 1, row) : (N - 1);   // last visible key
+        if (GEN ? (kbase + kTileRows - 1 > lim_blk) : ((kbase + kTileRows > Nk) || (CAUSAL && j == qb))) {
 #pragma unroll
           for (int q = 0; q < 128; ++q)
-            if (kbase + q > lim) s[q] = -INFINITY;
+            if (kbase + q > lim_row) s[q] = -INFINITY;
         }
         // row maximum: three-input max tree
         float m3[8];
@@ -415,8 +461,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float mx = fmax3(fmax3(m3[0], m3[1], m3[2]), fmax3(m3[3], m3[4], m3[5]), fmaxf(m3[6], m3[7]));
         const float mc = mx * scale_log2;
         const float m_new = (mc > m + kRescaleThreshold) ? mc : m;
-        const float alpha = ex2_approx(m - m_new);
-        const uint64_t nm2 = f2_pack(-m_new, -m_new);
+        // (a row that has seen no key yet keeps m = -inf: its P are 0 and alpha 1)
+        const float alpha = (GEN && m_new == m) ? 1.0f : ex2_approx(m - m_new);
+        const float nm = (GEN && m_new == -INFINITY) ? 0.0f : -m_new;
+        const uint64_t nm2 = f2_pack(nm, nm);
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};    // sum of P as computed (for lse)
         uint64_t accr[4] = {0ull, 0ull, 0ull, 0ull};   // d = 128: sum of P as rounded for the MMA
         uint32_t pk[64];
@@ -481,8 +529,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         reg_fence<16>(orr);
         lr = __uint_as_float(orr[0]);
       }
-      const float inv_l = 1.0f / lr;
-      uint8_t* orow = reinterpret_cast<uint8_t*>(out) + ((size_t)ti.bh * N + row) * (D * 2);
+      const float inv_l = (!GEN || lr > 0.0f) ? 1.0f / lr : 0.0f;   // a row that saw no key: O = 0
+      uint8_t* orow = reinterpret_cast<uint8_t*>(out) + ((size_t)ti.bh * Nq + row) * (D * 2);
 #pragma unroll
       for (int q = 0; q < D / 32; ++q) {
         uint32_t orr[32];
@@ -493,13 +541,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           w[i] = pack2<DT>(__uint_as_float(orr[2 * i]) * inv_l, __uint_as_float(orr[2 * i + 1]) * inv_l);
-        if (row < N) {
+        if (row < Nq) {
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             st_global_v4(orow + q * 64 + i * 16, w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
         }
       }
-      if (row < N) lse[(size_t)ti.bh * N + row] = (m + lg2_approx(l)) * 0.69314718055994530942f;
+      if (row < Nq) lse[(size_t)ti.bh * Nq + row] = (m + lg2_approx(l)) * 0.69314718055994530942f;
       tc_fence_before();
       mbar_arrive(bar(C::kOEmpty + t));
     }
@@ -518,7 +566,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // CTAs and keep the one whose busiest CTA has less work (adjacent on ties, since its
 // sub-tiles share more key/value loads).  With many tiles per CTA both balance well,
 // so the simulation is only run for small launches.
-int choose_balanced_pairing(int BH, int nqb, int grid) {
+int choose_balanced_pairing(int BH, int Nq, int Nk, int grid) {
+  const int nqb = (Nq + kTileRows - 1) / kTileRows;
   const int npairs = (nqb + 1) / 2;
   const long long ntiles = (long long)BH * npairs;
   if (ntiles > 8LL * grid) return 0;
@@ -536,7 +585,8 @@ int choose_balanced_pairing(int BH, int nqb, int grid) {
         qb0 = 2 * (npairs - 1 - (int)r);
         qb1 = qb0 + 1;
       }
-      const long long cost = (qb0 + 1) + ((qb1 < nqb && qb1 != qb0) ? qb1 + 1 : 0);
+      const long long cost = visible_kv_blocks(qb0, Nq, Nk, true) +
+                             ((qb1 < nqb && qb1 != qb0) ? visible_kv_blocks(qb1, Nq, Nk, true) : 0);
       const long long round = t / grid, pos = t % grid;
       load[(round & 1) ? grid - 1 - pos : pos] += cost;
     }
@@ -545,10 +595,10 @@ int choose_balanced_pairing(int BH, int nqb, int grid) {
   return worst[1] < worst[0] ? 1 : 0;
 }
 
-template <int D, int DT, bool CAUSAL>
+template <int D, int DT, bool CAUSAL, bool GEN>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   using C = FwdCfg<D>;
-  auto kern = fwd_kernel<D, DT, CAUSAL>;
+  auto kern = fwd_kernel<D, DT, CAUSAL, GEN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   // The register split inside the kernel must fit what the launch provides, or the
@@ -557,29 +607,34 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   e = cudaFuncGetAttributes(&attr, kern);
   if (e != cudaSuccess) return e;
   if (attr.numRegs * kThreads < (2 * kSoftmaxRegs + kOtherRegs) * 128) return cudaErrorInvalidConfiguration;
-  const int nqb = (a.N + kTileRows - 1) / kTileRows;
+  const int nqb = (a.Nq + kTileRows - 1) / kTileRows;
   const int ntiles = a.BH * ((nqb + 1) / 2);
   const int grid = ntiles < a.num_sms ? ntiles : a.num_sms;
-  const int balanced = CAUSAL ? choose_balanced_pairing(a.BH, nqb, grid) : 0;
+  const int balanced = CAUSAL ? choose_balanced_pairing(a.BH, a.Nq, a.Nk, grid) : 0;
   return launch_overlapped(kern, grid, kThreads, C::kSmemBytes, stream, a.tm_q, a.tm_k, a.tm_v,
-                           static_cast<uint16_t*>(a.o), a.lse, a.BH, a.N, a.scale_log2, balanced, a.err_word,
-                           a.limit_ns);
+                           static_cast<uint16_t*>(a.o), a.lse, a.BH, a.H, a.G, a.Nq, a.Nk, a.scale_log2, balanced,
+                           a.err_word, a.limit_ns);
+}
+
+template <bool GEN>
+cudaError_t launch_fwd_g(const FwdArgs& a, cudaStream_t stream) {
+  const int key = (a.d == 128 ? 4 : 0) | (a.dtype == 1 ? 2 : 0) | (a.causal ? 1 : 0);
+  switch (key) {
+    case 0: return launch_fwd_t<64, 0, false, GEN>(a, stream);
+    case 1: return launch_fwd_t<64, 0, true, GEN>(a, stream);
+    case 2: return launch_fwd_t<64, 1, false, GEN>(a, stream);
+    case 3: return launch_fwd_t<64, 1, true, GEN>(a, stream);
+    case 4: return launch_fwd_t<128, 0, false, GEN>(a, stream);
+    case 5: return launch_fwd_t<128, 0, true, GEN>(a, stream);
+    case 6: return launch_fwd_t<128, 1, false, GEN>(a, stream);
+    default: return launch_fwd_t<128, 1, true, GEN>(a, stream);
+  }
 }
 
 }  // namespace
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
-  const int key = (a.d == 128 ? 4 : 0) | (a.dtype == 1 ? 2 : 0) | (a.causal ? 1 : 0);
-  switch (key) {
-    case 0: return launch_fwd_t<64, 0, false>(a, stream);
-    case 1: return launch_fwd_t<64, 0, true>(a, stream);
-    case 2: return launch_fwd_t<64, 1, false>(a, stream);
-    case 3: return launch_fwd_t<64, 1, true>(a, stream);
-    case 4: return launch_fwd_t<128, 0, false>(a, stream);
-    case 5: return launch_fwd_t<128, 0, true>(a, stream);
-    case 6: return launch_fwd_t<128, 1, false>(a, stream);
-    default: return launch_fwd_t<128, 1, true>(a, stream);
-  }
+  return (a.Nq != a.Nk || a.G != 1) ? launch_fwd_g<true>(a, stream) : launch_fwd_g<false>(a, stream);
 }
 
 }  // namespace fa

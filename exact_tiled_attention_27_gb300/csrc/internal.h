@@ -15,10 +15,11 @@ constexpr unsigned int kErrTimeoutBit = 0x80000000u;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 struct FwdArgs {
-  CUtensorMap tm_q, tm_k, tm_v;  // 3-D maps {d, N, B*H}, box {64, 128, 1}, 128-byte swizzle
+  CUtensorMap tm_q;              // 3-D map {d, Nq, B*H}, box {64, 128, 1}, 128-byte swizzle
+  CUtensorMap tm_k, tm_v;        // 3-D maps {d, Nk, B*Hkv}, same box and swizzle
   void* o;
   float* lse;
-  int BH, N, d, dtype, causal;
+  int BH, H, G, Nq, Nk, d, dtype, causal;   // G = query heads per key/value head
   float scale_log2;              // scale * log2(e)
   unsigned int* err_word;
   uint64_t limit_ns;

@@ -96,6 +96,35 @@ def make_case(B, H, N, d, dtype="bf16", causal=False, scale=None, workload_index
     return Case(int(B), int(H), int(N), int(d), dtype, bool(causal), scale, q, k, v, do)
 
 
+@dataclass
+class CrossCase:
+    B: int
+    H: int
+    Hkv: int
+    Nq: int
+    Nk: int
+    d: int
+    dtype: str
+    causal: bool
+    scale: float
+    q: np.ndarray    # (B, H, Nq, d) 16-bit bits
+    k: np.ndarray    # (B, Hkv, Nk, d)
+    v: np.ndarray    # (B, Hkv, Nk, d)
+    do: np.ndarray   # (B, H, Nq, d) or None
+
+
+def make_cross_case(B, H, Hkv, Nq, Nk, d, dtype="bf16", causal=False, scale=None, workload_index=0,
+                    length_index=0, mult=1.0, with_do=True) -> CrossCase:
+    """Seeded Q (B, H, Nq, d), K and V (B, Hkv, Nk, d) (x ``mult``) and dO (unscaled)."""
+    scale = float(d) ** -0.5 if scale is None else float(scale)
+    qs, ks = (int(B), int(H), int(Nq), int(d)), (int(B), int(Hkv), int(Nk), int(d))
+    q = gaussian_bits(qs, seed_for(workload_index, length_index, "q"), dtype, mult)
+    k = gaussian_bits(ks, seed_for(workload_index, length_index, "k"), dtype, mult)
+    v = gaussian_bits(ks, seed_for(workload_index, length_index, "v"), dtype, mult)
+    do = gaussian_bits(qs, seed_for(workload_index, length_index, "do"), dtype) if with_do else None
+    return CrossCase(int(B), int(H), int(Hkv), int(Nq), int(Nk), int(d), dtype, bool(causal), scale, q, k, v, do)
+
+
 # The workloads, as (name, B, H, N, d, dtype, causal, backward, mult).  The sweep
 # entries keep B*N = 65536 tokens.
 WORKLOADS = {

@@ -88,6 +88,27 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int B, int H, int N, int d, float scale, int causal, int dtype, void* stream);
 
 /*
+ * Forward with different query and key lengths and with grouped key/value heads.
+ *   q, o  : [B, H, Nq, d];   k, v : [B, Hkv, Nk, d];   lse : [B, H, Nq] float32.
+ *   Query head h reads key/value head h / (H / Hkv) (Hkv must divide H; Hkv = H is
+ *   ordinary multi-head attention, Hkv = 1 multi-query attention).
+ *   causal : the mask is aligned bottom-right: query row i sees key j iff
+ *            j <= i + (Nk - Nq), so the last query row is the newest token and
+ *            Nq = Nk gives fa_fwd's mask.  When Nk < Nq the first Nq - Nk rows see no
+ *            key; their O rows are 0 and their lse is -inf.
+ * Everything else (layout, alignment, dtype, scale, stream, errors; FA_ERR_SHAPE
+ * also when Hkv does not divide H) is as for fa_fwd, which is this call with
+ * Hkv = H and Nq = Nk = N.  The pages define attention for one sequence length; the
+ * cross lengths, the bottom-right alignment and the head grouping are this
+ * library's reading (the practitioner article, section 3.1, decodes new tokens
+ * against a key/value cache; "大模型数学速成（17）", section 五, names grouped-query
+ * attention as orthogonal to the tiling).
+ */
+int fa_fwd_cross(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                 int dtype, void* stream);
+
+/*
  * Bytes of device scratch that fa_bwd needs for these sizes: the per-row
  * D = rowsum(dO o O) and the row log-sum-exp in base 2 (both padded to whole
  * 128-row blocks), plus a float32 dQ accumulator of B*H*N*d elements.

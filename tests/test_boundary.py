@@ -83,6 +83,24 @@ def test_forward_validation_codes(lib):
     assert fwd(lib, o=PM) == C["FA_ERR_ALIGN"]
 
 
+def fwd_cross(lib, q=P, k=P, B=1, H=4, Hkv=2, Nq=3, Nk=300, d=64, scale=0.125, causal=1, dtype=0):
+    return lib.fa_fwd_cross(q, k, P, P, P, B, H, Hkv, Nq, Nk, d, scale, causal, dtype, NULL)
+
+
+def test_forward_cross_validation_codes(lib):
+    C = binding.STATUS_CODE
+    assert fwd_cross(lib, Hkv=3) == C["FA_ERR_SHAPE"]          # 3 does not divide 4
+    assert fwd_cross(lib, Hkv=0) == C["FA_ERR_SHAPE"]
+    assert fwd_cross(lib, Hkv=8) == C["FA_ERR_SHAPE"]          # more key/value heads than query heads
+    assert fwd_cross(lib, Nq=0) == C["FA_ERR_SHAPE"]
+    assert fwd_cross(lib, Nk=0) == C["FA_ERR_SHAPE"]
+    assert fwd_cross(lib, d=80) == C["FA_ERR_UNSUPPORTED_D"]
+    assert fwd_cross(lib, dtype=5) == C["FA_ERR_DTYPE"]
+    assert fwd_cross(lib, scale=0.0) == C["FA_ERR_SCALE"]
+    assert fwd_cross(lib, q=NULL) == C["FA_ERR_NULL"]
+    assert fwd_cross(lib, k=PM) == C["FA_ERR_ALIGN"]
+
+
 def test_backward_validation_codes(lib):
     C = binding.STATUS_CODE
     assert bwd(lib, dtype=7) == C["FA_ERR_DTYPE"]
@@ -107,6 +125,7 @@ def test_valid_arguments_without_gpu_report_no_device(lib):
     except ImportError:
         pass
     assert fwd(lib) == binding.STATUS_CODE["FA_ERR_NO_DEVICE"]
+    assert fwd_cross(lib) == binding.STATUS_CODE["FA_ERR_NO_DEVICE"]
     assert bwd(lib) == binding.STATUS_CODE["FA_ERR_NO_DEVICE"]
     assert lib.fa_get_last_kernel_status(NULL) == binding.STATUS_CODE["FA_ERR_NO_DEVICE"]
 
