@@ -59,6 +59,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             fn = getattr(lib, name)
             fn.argtypes = lib.fa_bwd.argtypes
             fn.restype = i
+        lib.fa_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, f, i, i, vp]
+        lib.fa_bwd_gqa.restype = i
         lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
         lib.fa_bwd_noalloc.restype = i
         lib.fa_bwd_noalloc_max_scratch.argtypes = []
@@ -177,25 +179,33 @@ def forward_cross(q, k, v, scale=None, causal=False, out=None, lse=None, stream=
 
 def backward(q, k, v, o, do, lse, scale=None, causal=False, dq=None, dk=None, dv=None, workspace=None,
              stream=None, stage=None):
-    """Exact attention backward.  Returns (dq, dk, dv) like q.
+    """Exact attention backward.  Returns (dq, dk, dv): dq like q, dk and dv like k.
 
-    ``workspace`` (optional) is a CUDA uint8 tensor of at least workspace_size(B,H,N,d)
-    bytes; one is allocated through torch when it is not given.  ``stage`` runs one of
-    the three launches of the backward ("preprocess", "dkdv", "dq_convert"); calling the
-    three in order with the same workspace equals the default (all three).
+    k and v may have fewer heads than q (grouped key/value heads, Hkv dividing H);
+    dk and dv then sum over the query heads of each group.  ``workspace`` (optional)
+    is a CUDA uint8 tensor of at least workspace_size(B,H,N,d) bytes; one is allocated
+    through torch when it is not given.  ``stage`` runs one of the three launches of
+    the backward ("preprocess", "dkdv", "dq_convert"; Hkv = H only); calling the three
+    in order with the same workspace equals the default (all three).
     """
     torch = _torch()
     B, H, N, d = q.shape
-    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
+    Hkv = int(k.shape[1])
+    for name, t in (("q", q), ("o", o), ("do", do)):
         _check_bhnd(name, t, (B, H, N, d), q.dtype)
+    for name, t in (("k", k), ("v", v)):
+        _check_bhnd(name, t, (B, Hkv, N, d), q.dtype)
+    if Hkv != H and stage is not None:
+        raise ValueError("the single-stage calls take Hkv == H")
     if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous float32 (B, H, N) tensor")
     scale = float(d) ** -0.5 if scale is None else float(scale)
     dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(q) if dk is None else dk
-    dv = torch.empty_like(q) if dv is None else dv
-    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
-        _check_bhnd(name, t, (B, H, N, d), q.dtype)
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check_bhnd("dq", dq, (B, H, N, d), q.dtype)
+    for name, t in (("dk", dk), ("dv", dv)):
+        _check_bhnd(name, t, (B, Hkv, N, d), q.dtype)
     need = workspace_size(B, H, N, d)
     fn_name = {None: "fa_bwd", "preprocess": "fa_bwd_preprocess", "dkdv": "fa_bwd_dkdv",
                "dq_convert": "fa_bwd_dq_convert"}[stage]
@@ -203,6 +213,14 @@ def backward(q, k, v, o, do, lse, scale=None, causal=False, dq=None, dk=None, dv
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     if workspace.numel() * workspace.element_size() < need:
         raise ValueError(f"workspace too small: need {need} bytes")
+    if Hkv != H:
+        fn_name = "fa_bwd_gqa"
+        st = load_library().fa_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
+                                       _ptr(dv), _ptr(workspace), need, B, H, Hkv, N, d, scale, 1 if causal else 0,
+                                       _dtype_code(q), _stream_handle(stream))
+        if st != 0:
+            raise FaError(st, fn_name)
+        return dq, dk, dv
     fn = getattr(load_library(), fn_name)
     st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
             _ptr(workspace), need, B, H, N, d, scale, 1 if causal else 0, _dtype_code(q), _stream_handle(stream))

@@ -211,10 +211,11 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
 }
 
 static int bwd_common(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
-                      void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes, int B, int H, int N, int d,
-                      float scale, int causal, int dtype, void* stream, int stages) {
+                      void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes, int B, int H, int Hkv, int N,
+                      int d, float scale, int causal, int dtype, void* stream, int stages) {
   int st = check_common(B, H, N, d, scale, dtype);
   if (st != FA_OK) return st;
+  if (Hkv < 1 || Hkv > H || H % Hkv != 0) return FA_ERR_SHAPE;
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_NULL;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) || !aligned16(dq) ||
       !aligned16(dk) || !aligned16(dv) || (reinterpret_cast<uintptr_t>(lse) & 3u))
@@ -227,8 +228,8 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
   if (st != FA_OK) return st;
   BwdArgs a;
   const int BH = B * H;
-  if (!encode_bhnd(&a.tm_q, q, BH, N, d, dtype) || !encode_bhnd(&a.tm_k, k, BH, N, d, dtype) ||
-      !encode_bhnd(&a.tm_v, v, BH, N, d, dtype) || !encode_bhnd(&a.tm_do, dO, BH, N, d, dtype))
+  if (!encode_bhnd(&a.tm_q, q, BH, N, d, dtype) || !encode_bhnd(&a.tm_k, k, B * Hkv, N, d, dtype) ||
+      !encode_bhnd(&a.tm_v, v, B * Hkv, N, d, dtype) || !encode_bhnd(&a.tm_do, dO, BH, N, d, dtype))
     return FA_ERR_LAUNCH;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.o = o;
@@ -243,6 +244,9 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
   a.dq_accum = reinterpret_cast<float*>(ws + w.acc_off);
   if (!encode_accum(&a.tm_dq, a.dq_accum, BH, N, d)) return FA_ERR_LAUNCH;
   a.BH = BH;
+  a.BHkv = B * Hkv;
+  a.H = H;
+  a.G = H / Hkv;
   a.N = N;
   a.Npad = w.Npad;
   a.d = d;
@@ -253,37 +257,45 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
   a.err_word = dev->err_word;
   a.limit_ns = kWaitLimitNs;
   a.num_sms = dev->num_sms;
-  // every key block re-reads the head's Q and dO (16-bit) and adds into its float32 dQ
-  a.heads_per_group = heads_per_group(8LL * N * d, dev->l2_bytes, BH);
+  // every key block re-reads the Q and dO (16-bit) of the key/value head's G query heads
+  // and adds into their float32 dQ
+  a.heads_per_group = heads_per_group(8LL * a.G * N * d, dev->l2_bytes, a.BHkv);
   return launch_bwd(a, static_cast<cudaStream_t>(stream), stages) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse, void* dq,
            void* dk, void* dv, void* workspace, size_t ws_bytes, int B, int H, int N, int d, float scale, int causal,
            int dtype, void* stream) {
-  return bwd_common(q, k, v, o, dO, lse, dq, dk, dv, workspace, ws_bytes, B, H, N, d, scale, causal, dtype, stream,
+  return bwd_common(q, k, v, o, dO, lse, dq, dk, dv, workspace, ws_bytes, B, H, H, N, d, scale, causal, dtype, stream,
                     kBwdStagePre | kBwdStageKV | kBwdStageDQ);
 }
 
 int fa_bwd_preprocess(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                       void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes, int B, int H, int N, int d,
                       float scale, int causal, int dtype, void* stream) {
-  return bwd_common(q, k, v, o, dO, lse, dq, dk, dv, workspace, ws_bytes, B, H, N, d, scale, causal, dtype, stream,
+  return bwd_common(q, k, v, o, dO, lse, dq, dk, dv, workspace, ws_bytes, B, H, H, N, d, scale, causal, dtype, stream,
                     kBwdStagePre);
 }
 
 int fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                 void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes, int B, int H, int N, int d,
                 float scale, int causal, int dtype, void* stream) {
-  return bwd_common(q, k, v, o, dO, lse, dq, dk, dv, workspace, ws_bytes, B, H, N, d, scale, causal, dtype, stream,
+  return bwd_common(q, k, v, o, dO, lse, dq, dk, dv, workspace, ws_bytes, B, H, H, N, d, scale, causal, dtype, stream,
                     kBwdStageKV);
 }
 
 int fa_bwd_dq_convert(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                       void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes, int B, int H, int N, int d,
                       float scale, int causal, int dtype, void* stream) {
-  return bwd_common(q, k, v, o, dO, lse, dq, dk, dv, workspace, ws_bytes, B, H, N, d, scale, causal, dtype, stream,
+  return bwd_common(q, k, v, o, dO, lse, dq, dk, dv, workspace, ws_bytes, B, H, H, N, d, scale, causal, dtype, stream,
                     kBwdStageDQ);
+}
+
+int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+               void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes, int B, int H, int Hkv, int N, int d,
+               float scale, int causal, int dtype, void* stream) {
+  return bwd_common(q, k, v, o, dO, lse, dq, dk, dv, workspace, ws_bytes, B, H, Hkv, N, d, scale, causal, dtype,
+                    stream, kBwdStagePre | kBwdStageKV | kBwdStageDQ);
 }
 
 const char* fa_strerror(int status) {

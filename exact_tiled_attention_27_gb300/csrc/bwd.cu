@@ -108,13 +108,16 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int u) {
   return static_cast<uint32_t>(r * 128 + ((u ^ (r & 7)) << 4));
 }
 
-template <int D, int DT, bool CAUSAL>
+// GQA: key/value heads shared by groups of G > 1 query heads (fa_bwd_gqa); otherwise
+// G = 1 and the query head is the key/value head.
+template <int D, int DT, bool CAUSAL, bool GQA>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ nlse2, const float* __restrict__ ndvec, float* __restrict__ dq_accum,
                   unsigned int* __restrict__ tile_counter,
-                  uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, int BH, int N, int Npad, float scale,
+                  uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, int BHkv, int H, int G, int N, int Npad,
+                  float scale,
                   float scale_log2, int hg, unsigned int* err_word, uint64_t limit_ns) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -129,7 +132,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // warp index through a shuffle so the compiler can treat it as warp-uniform
   const int warp = __shfl_sync(0xffffffffu, threadIdx.x >> 5, 0);
   const int nb = (N + kRows - 1) / kRows;
-  const int ntiles = BH * nb;
+  const int ntiles = BHkv * nb;   // (batch x key/value head, key block)
+  // The query heads that read key/value head bhk are G consecutive heads starting at
+  // first_q_head(bhk); a tile's steps run over all of their query blocks, so dK and dV
+  // sum over the group in tensor memory.  G = 1 is ordinary multi-head attention.
+  auto first_q_head = [&](int bhk) { return GQA ? (bhk / (H / G)) * H + (bhk % (H / G)) * G : bhk; };
+  const int group = GQA ? G : 1;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kKVBufs; ++i) {
@@ -213,7 +221,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         __syncwarp();
         if (tile < 0) break;
         int kb, bh;                        // key block: kb = 0 carries the most query blocks (causal)
-        group_order(tile, BH, nb, hg, kb, bh);
+        group_order(tile, BHkv, nb, hg, kb, bh);
         const int kvb = it % C::kKVBufs;
         if (it >= C::kKVBufs && !wait_warp(bar(C::kKVEmpty + kvb), ((it / C::kKVBufs) - 1) & 1, ctl, 0x401)) {
           ok = false;
@@ -231,6 +239,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         __syncwarp();
         const int q0 = CAUSAL ? kb : 0;
+        for (int g = 0; ok && g < group; ++g) {
+        const int bhq = first_q_head(bh) + g;
         for (int qi = q0; qi < nb; ++qi, ++s) {
           const int qs = s % C::kQBufs;
           if (s >= (uint32_t)C::kQBufs && !wait_warp(bar(C::kQEmpty + qs), ((s / C::kQBufs) - 1) & 1, ctl, 0x402)) {
@@ -244,14 +254,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_arrive_expect_tx(bar(C::kQFull + qs), 2 * C::kTileBytes + 2 * kRows * 4);
 #pragma unroll
             for (int c = 0; c < C::kChunks; ++c) {
-              tma_load_3d(qdst + c * kChunkBytes, &tm_q, bar(C::kQFull + qs), c * 64, qi * kRows, bh);
-              tma_load_3d(odst + c * kChunkBytes, &tm_do, bar(C::kQFull + qs), c * 64, qi * kRows, bh);
+              tma_load_3d(qdst + c * kChunkBytes, &tm_q, bar(C::kQFull + qs), c * 64, qi * kRows, bhq);
+              tma_load_3d(odst + c * kChunkBytes, &tm_do, bar(C::kQFull + qs), c * 64, qi * kRows, bhq);
             }
-            const size_t srow = (size_t)bh * Npad + (size_t)qi * kRows;
+            const size_t srow = (size_t)bhq * Npad + (size_t)qi * kRows;
             bulk_load(stats, nlse2 + srow, kRows * 4, bar(C::kQFull + qs));
             bulk_load(stats + kRows * 4, ndvec + srow, kRows * 4, bar(C::kQFull + qs));
           }
           __syncwarp();
+        }
         }
         if (!ok) {
           ++it;   // this tile's K and V were issued: the drain below must wait for them
@@ -310,10 +321,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int tile = take_tile(it, 0x50f);
         if (tile < 0) break;
         int kb, bh;
-        group_order(tile, BH, nb, hg, kb, bh);
+        group_order(tile, BHkv, nb, hg, kb, bh);
         const int kvb = it % C::kKVBufs;
         const int q0 = CAUSAL ? kb : 0;
-        const int nsteps = nb - q0;
+        const int nsteps = group * (nb - q0);
         if (!wait_warp(bar(C::kKVFull + kvb), (it / C::kKVBufs) & 1, ctl, 0x501)) break;
         const uint32_t kbase = smem_u32(smem + C::kOffK + kvb * C::kTileBytes);
         const uint32_t vbase = smem_u32(smem + C::kOffV + kvb * C::kTileBytes);
@@ -433,9 +444,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int tile = take_tile(k, 0x60f);
       if (tile < 0) break;
       int kb, bh;
-      group_order(tile, BH, nb, hg, kb, bh);
+      group_order(tile, BHkv, nb, hg, kb, bh);
       const int q0 = CAUSAL ? kb : 0;
       bool ok = true;
+      for (int g = 0; ok && g < group; ++g)
       for (int qi = q0; qi < nb; ++qi, ++s) {
         const int qs = s % C::kQBufs;
         bool w = mbar_wait(bar(C::kSFull), s & 1, ctl, 0x601);
@@ -547,9 +559,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int tile = take_tile(it, 0x70f);
       if (tile < 0) break;
       int kb, bh;
-      group_order(tile, BH, nb, hg, kb, bh);
+      group_order(tile, BHkv, nb, hg, kb, bh);
       const int q0 = CAUSAL ? kb : 0;
       bool ok = true;
+      for (int g = 0; ok && g < group; ++g) {
+      const int bhq = first_q_head(bh) + g;
       for (int qi = q0; qi < nb; ++qi, ++s) {
         if (!wait_warp(bar(C::kDQFull), s & 1, ctl, 0x701)) {
           ok = false;
@@ -558,7 +572,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // d = 64: the next tile's first gradient MMAs wait for the dK/dV columns, so
         // those are read out before the last dQ of the tile (at d = 128 the next
         // tile's first scores wait for the dQ columns instead, so dQ goes first)
-        if (C::kEarly && qi == nb - 1 && !write_dkdv(it, kb, bh)) {
+        if (C::kEarly && g == group - 1 && qi == nb - 1 && !write_dkdv(it, kb, bh)) {
           ok = false;
           break;
         }
@@ -590,7 +604,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
               for (int c = 0; c < 2; ++c)
                 tma_reduce_add_3d(&tm_dq, smem_u32(smem + C::kOffDQS + c * kChunkBytes), (half * 2 + c) * 32,
-                                  qi * kRows, bh);
+                                  qi * kRows, bhq);
               bulk_commit_group();
               bulk_wait_read_all();   // the staging tile may be overwritten after this
             }
@@ -598,6 +612,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           named_bar_sync(1, 128);
         }
+      }
       }
       if (!ok) break;
       if (!C::kEarly && !write_dkdv(it, kb, bh)) break;
@@ -682,7 +697,7 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ a
   }
 }
 
-template <int D, int DT, bool CAUSAL>
+template <int D, int DT, bool CAUSAL, bool GQA>
 cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int stages) {
   using C = BwdCfg<D>;
   if (stages & kBwdStagePre) {
@@ -698,7 +713,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int stages) {
     if (e != cudaSuccess) return e;
   }
   if (stages & kBwdStageKV) {
-    auto kern = bwd_kv_kernel<D, DT, CAUSAL>;
+    auto kern = bwd_kv_kernel<D, DT, CAUSAL, GQA>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     // the setmaxnreg split inside the kernel must fit what the launch provides
@@ -707,11 +722,11 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int stages) {
     if (e != cudaSuccess) return e;
     if (attr.numRegs * kBwdThreads < (2 * kDsRegs + kDqRegs + kCtlRegs) * 128) return cudaErrorInvalidConfiguration;
     const int nb = (a.N + kRows - 1) / kRows;
-    const int ntiles = a.BH * nb;
+    const int ntiles = a.BHkv * nb;
     const int grid = ntiles < a.num_sms ? ntiles : a.num_sms;
     e = launch_overlapped(kern, grid, kBwdThreads, C::kSmemBytes, stream, a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dq,
                           a.lse2, a.dvec, a.dq_accum, a.tile_counter, static_cast<uint16_t*>(a.dk),
-                          static_cast<uint16_t*>(a.dv), a.BH, a.N, a.Npad, a.scale, a.scale_log2,
+                          static_cast<uint16_t*>(a.dv), a.BHkv, a.H, a.G, a.N, a.Npad, a.scale, a.scale_log2,
                           a.heads_per_group, a.err_word, a.limit_ns);
     if (e != cudaSuccess) return e;
   }
@@ -726,20 +741,25 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int stages) {
   return cudaSuccess;
 }
 
+template <bool GQA>
+cudaError_t launch_bwd_g(const BwdArgs& a, cudaStream_t stream, int stages) {
+  const int key = (a.d == 128 ? 4 : 0) | (a.dtype == 1 ? 2 : 0) | (a.causal ? 1 : 0);
+  switch (key) {
+    case 0: return launch_bwd_t<64, 0, false, GQA>(a, stream, stages);
+    case 1: return launch_bwd_t<64, 0, true, GQA>(a, stream, stages);
+    case 2: return launch_bwd_t<64, 1, false, GQA>(a, stream, stages);
+    case 3: return launch_bwd_t<64, 1, true, GQA>(a, stream, stages);
+    case 4: return launch_bwd_t<128, 0, false, GQA>(a, stream, stages);
+    case 5: return launch_bwd_t<128, 0, true, GQA>(a, stream, stages);
+    case 6: return launch_bwd_t<128, 1, false, GQA>(a, stream, stages);
+    default: return launch_bwd_t<128, 1, true, GQA>(a, stream, stages);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream, int stages) {
-  const int key = (a.d == 128 ? 4 : 0) | (a.dtype == 1 ? 2 : 0) | (a.causal ? 1 : 0);
-  switch (key) {
-    case 0: return launch_bwd_t<64, 0, false>(a, stream, stages);
-    case 1: return launch_bwd_t<64, 0, true>(a, stream, stages);
-    case 2: return launch_bwd_t<64, 1, false>(a, stream, stages);
-    case 3: return launch_bwd_t<64, 1, true>(a, stream, stages);
-    case 4: return launch_bwd_t<128, 0, false>(a, stream, stages);
-    case 5: return launch_bwd_t<128, 0, true>(a, stream, stages);
-    case 6: return launch_bwd_t<128, 1, false>(a, stream, stages);
-    default: return launch_bwd_t<128, 1, true>(a, stream, stages);
-  }
+  return a.G != 1 ? launch_bwd_g<true>(a, stream, stages) : launch_bwd_g<false>(a, stream, stages);
 }
 
 }  // namespace fa

@@ -27,7 +27,8 @@ struct FwdArgs {
 };
 
 struct BwdArgs {
-  CUtensorMap tm_q, tm_k, tm_v, tm_do;
+  CUtensorMap tm_q, tm_do;       // {d, N, B*H}
+  CUtensorMap tm_k, tm_v;        // {d, N, B*Hkv}
   CUtensorMap tm_dq;  // 3-D map {d, N, B*H} over the float32 dQ accumulator, box {32, 128, 1}
   const void* o;
   const void* dO;
@@ -39,7 +40,8 @@ struct BwdArgs {
   float* lse2;        // [B*H*Npad]  lse * log2(e), +inf on padding rows
   float* dq_accum;    // [B*H*N*d]   float32 dQ partial sums
   unsigned int* tile_counter;  // tiles handed out beyond the first one per CTA
-  int BH, N, Npad, d, dtype, causal;
+  int BH, N, Npad, d, dtype, causal;   // BH = B*H query heads
+  int BHkv, H, G;                      // B*Hkv key/value heads; G = H / Hkv query heads per key/value head
   float scale, scale_log2;
   unsigned int* err_word;
   uint64_t limit_ns;

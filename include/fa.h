@@ -141,6 +141,22 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            int B, int H, int N, int d, float scale, int causal, int dtype, void* stream);
 
 /*
+ * Backward with grouped key/value heads (square N): the gradients of fa_fwd_cross
+ * with Nq = Nk = N.
+ *   q, o, dO, dq : [B, H, N, d];   k, v, dk, dv : [B, Hkv, N, d];   lse : [B, H, N].
+ *   Query head h reads key/value head h / (H / Hkv); dk and dv of a key/value head
+ *   are the sums of the per-query-head gradients over the H / Hkv query heads that
+ *   read it (accumulated on chip, written once).  The workspace is
+ *   fa_bwd_workspace_size(B, H, N, d).  Everything else, including the errors
+ *   (FA_ERR_SHAPE also when Hkv does not divide H), is as for fa_bwd, which is this
+ *   call with Hkv = H.
+ */
+int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dO,
+               const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+               int B, int H, int Hkv, int N, int d, float scale, int causal, int dtype,
+               void* stream);
+
+/*
  * The three stages fa_bwd runs, one launch each, for callers that want to time or
  * schedule them separately.  Arguments, validation and errors are exactly fa_bwd's;
  * calling the three in this order on one stream with one workspace is fa_bwd.

@@ -101,6 +101,20 @@ def test_forward_cross_validation_codes(lib):
     assert fwd_cross(lib, k=PM) == C["FA_ERR_ALIGN"]
 
 
+def test_backward_gqa_validation_codes(lib):
+    C = binding.STATUS_CODE
+    need = lib.fa_bwd_workspace_size(1, 4, 128, 64)
+
+    def call(H=4, Hkv=2, N=128, ws_bytes=need):
+        return lib.fa_bwd_gqa(P, P, P, P, P, P, P, P, P, P, ws_bytes, 1, H, Hkv, N, 64, 0.125, 1, 0, NULL)
+
+    assert call(Hkv=3) == C["FA_ERR_SHAPE"]
+    assert call(Hkv=0) == C["FA_ERR_SHAPE"]
+    assert call(Hkv=8) == C["FA_ERR_SHAPE"]
+    assert call(N=0) == C["FA_ERR_SHAPE"]
+    assert call(ws_bytes=need - 1) == C["FA_ERR_WORKSPACE"]
+
+
 def test_backward_validation_codes(lib):
     C = binding.STATUS_CODE
     assert bwd(lib, dtype=7) == C["FA_ERR_DTYPE"]

@@ -9,7 +9,7 @@ import pytest
 torch = pytest.importorskip("torch")
 
 import oracle  # noqa: E402
-from exact_tiled_attention_27_gb300 import build, forward, forward_cross, last_kernel_status  # noqa: E402
+from exact_tiled_attention_27_gb300 import backward, build, forward, forward_cross, last_kernel_status  # noqa: E402
 from exact_tiled_attention_27_gb300.inputs import bits_to_f64, make_case, make_cross_case  # noqa: E402
 from tests import gpu_util as G  # noqa: E402
 
@@ -82,3 +82,31 @@ def test_grouped_heads_equal_repeated_heads():
                      causal=True)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+GQA_BWD_CASES = [
+    # B, H, Hkv, N, d, dtype, causal
+    (1, 4, 2, 300, 64, "bf16", True),
+    (2, 6, 3, 256, 64, "fp16", False),
+    (1, 8, 1, 200, 128, "bf16", True),
+    (1, 4, 4, 129, 128, "fp16", True),    # Hkv = H: the same call takes the ordinary path
+]
+
+
+@pytest.mark.parametrize("B,H,Hkv,N,d,dtype,causal", GQA_BWD_CASES)
+def test_grouped_backward_matches_oracle(B, H, Hkv, N, d, dtype, causal):
+    c = make_cross_case(B, H, Hkv, N, N, d, dtype, causal, workload_index=203, length_index=N + H)
+    q, k, v, do = (G.to_device(getattr(c, n), dtype) for n in ("q", "k", "v", "do"))
+    o, lse = forward_cross(q, k, v, scale=c.scale, causal=causal)
+    dq, dk, dv = backward(q, k, v, o, do, lse, scale=c.scale, causal=causal)
+    torch.cuda.synchronize()
+    assert last_kernel_status() == 0
+    q64, k64, v64, do64 = (bits_to_f64(getattr(c, n), dtype) for n in ("q", "k", "v", "do"))
+    refs = oracle.attn_gqa_bwd_ref(q64, k64, v64, do64, c.scale, causal)
+    for b in range(B):
+        for hk in range(Hkv):
+            G.check_backward([np.zeros(1), G.to_f64(dk[b, hk]), G.to_f64(dv[b, hk])],
+                             [np.zeros(1), refs[1][b, hk], refs[2][b, hk]], f"gqa dK/dV ({b},{hk})")
+        for h in range(H):
+            err = G.rel_l2(G.to_f64(dq[b, h]), refs[0][b, h])
+            assert err <= G.GRAD_RELL2, f"dQ ({b},{h}) relL2 {err:.3e}"
