@@ -18,6 +18,8 @@ from .binding import (  # noqa: F401
     FaError,
     backward,
     debug_wait_timeout,
+    decode,
+    decode_workspace_size,
     device_sm_count,
     forward,
     forward_cross,

@@ -59,6 +59,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             fn = getattr(lib, name)
             fn.argtypes = lib.fa_bwd.argtypes
             fn.restype = i
+        lib.fa_decode_workspace_size.argtypes = [i, i, i, i, i, i]
+        lib.fa_decode_workspace_size.restype = sz
+        lib.fa_decode.argtypes = [vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, f, i, i, vp]
+        lib.fa_decode.restype = i
         lib.fa_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, f, i, i, vp]
         lib.fa_bwd_gqa.restype = i
         lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
@@ -175,6 +179,40 @@ def forward_cross(q, k, v, scale=None, causal=False, out=None, lse=None, stream=
     if st != 0:
         raise FaError(st, "fa_fwd_cross")
     return out, lse
+
+
+def decode(q, k, v, scale=None, causal=True, out=None, lse=None, workspace=None, stream=None):
+    """Split-key decode for a few query rows: q (B, H, Nq, d), k, v (B, Hkv, Nk, d)
+    with (H / Hkv) * Nq <= 8.  Same result as ``forward_cross``; returns (o, lse).
+    ``workspace`` (optional) is a CUDA uint8 tensor of at least
+    ``decode_workspace_size(...)`` bytes."""
+    torch = _torch()
+    B, H, Nq, d = q.shape
+    Hkv, Nk = int(k.shape[1]), int(k.shape[2])
+    _check_bhnd("q", q, (B, H, Nq, d), q.dtype)
+    _check_bhnd("k", k, (B, Hkv, Nk, d), q.dtype)
+    _check_bhnd("v", v, (B, Hkv, Nk, d), q.dtype)
+    scale = float(d) ** -0.5 if scale is None else float(scale)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check_bhnd("out", out, (B, H, Nq, d), q.dtype)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, Nq) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 (B, H, Nq) tensor")
+    lib = load_library()
+    need = int(lib.fa_decode_workspace_size(B, H, Hkv, Nq, Nk, d))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = _ptr(workspace) if workspace is not None else ctypes.c_void_p(0)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib.fa_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), ws_ptr, ws_bytes, B, H, Hkv, Nq, Nk, d,
+                       scale, 1 if causal else 0, _dtype_code(q), _stream_handle(stream))
+    if st != 0:
+        raise FaError(st, "fa_decode")
+    return out, lse
+
+
+def decode_workspace_size(B, H, Hkv, Nq, Nk, d) -> int:
+    return int(load_library().fa_decode_workspace_size(B, H, Hkv, Nq, Nk, d))
 
 
 def backward(q, k, v, o, do, lse, scale=None, causal=False, dq=None, dk=None, dv=None, workspace=None,

@@ -24,7 +24,7 @@ BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libfa_gb300.so")
 
-SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "decode.cu", "noalloc.cu"]
 HEADERS = ["ptx.cuh", "internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",

@@ -298,6 +298,77 @@ int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const
                     stream, kBwdStagePre | kBwdStageKV | kBwdStageDQ);
 }
 
+// ---------------------------------------------------------------- split-key decode
+// Ranges hold at least 256 keys; at most 128 ranges.
+static int decode_max_splits(int Nk) {
+  int s = Nk / 256;
+  return s < 1 ? 1 : (s > 128 ? 128 : s);
+}
+
+static int decode_check(int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int dtype) {
+  int st = check_common(B, H, Nq, d, scale, dtype);
+  if (st != FA_OK) return st;
+  if (Hkv < 1 || Hkv > H || H % Hkv != 0) return FA_ERR_SHAPE;
+  st = check_common(B, Hkv, Nk, d, scale, dtype);
+  if (st != FA_OK) return st;
+  if ((long long)(H / Hkv) * Nq > kDecodeMaxRows) return FA_ERR_SHAPE;
+  return FA_OK;
+}
+
+size_t fa_decode_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int d) {
+  if (decode_check(B, H, Hkv, Nq, Nk, d, 1.0f, FA_BF16) != FA_OK) return 0;
+  const int smax = decode_max_splits(Nk);
+  if (smax == 1) return 0;
+  const size_t rows = (size_t)smax * B * Hkv * (H / Hkv) * Nq;
+  return round_up(rows * d * 4) + round_up(rows * 4);
+}
+
+int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace, size_t ws_bytes,
+              int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int causal, int dtype, void* stream) {
+  int st = decode_check(B, H, Hkv, Nq, Nk, d, scale, dtype);
+  if (st != FA_OK) return st;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return FA_ERR_ALIGN;
+  const size_t need = fa_decode_workspace_size(B, H, Hkv, Nq, Nk, d);
+  if (need > 0 && (workspace == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1))))
+    return FA_ERR_WORKSPACE;
+  DeviceInfo* dev = nullptr;
+  st = get_device(&dev);
+  if (st != FA_OK) return st;
+  DecArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.BHkv = B * Hkv;
+  a.H = H;
+  a.Hkv = Hkv;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.M = (H / Hkv) * Nq;
+  a.d = d;
+  a.dtype = dtype;
+  a.causal = causal ? 1 : 0;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  // enough ranges for about three CTAs per SM, each range a whole number of CTA steps
+  const int smax = decode_max_splits(Nk);
+  long long want = (3LL * dev->num_sms + a.BHkv - 1) / a.BHkv;
+  if (want < 1) want = 1;
+  if (want > smax) want = smax;
+  const int kps = decode_keys_per_step(d);
+  int chunk = (int)((Nk + want - 1) / want);
+  chunk = (chunk + kps - 1) / kps * kps;
+  a.chunk = chunk;
+  a.S = (Nk + chunk - 1) / chunk;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t rows = (size_t)a.S * a.BHkv * a.M;
+  a.opart = a.S > 1 ? reinterpret_cast<float*>(ws) : nullptr;
+  a.lpart = a.S > 1 ? reinterpret_cast<float*>(ws + round_up(rows * d * 4)) : nullptr;
+  return launch_decode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
 const char* fa_strerror(int status) {
   switch (status) {
     case FA_OK: return "ok";

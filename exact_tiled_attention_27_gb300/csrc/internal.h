@@ -76,11 +76,11 @@ inline int heads_per_group(long long bytes_per_head, long long l2_bytes, int BH)
 // previous kernel in the stream drains; every kernel here calls grid_dep_wait before
 // it reads or writes global memory.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_overlapped(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem,
-                              cudaStream_t stream, Args... args) {
+cudaError_t launch_overlapped(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args... args) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(block);
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -92,6 +92,24 @@ cudaError_t launch_overlapped(void (*kern)(KArgs...), unsigned grid, unsigned bl
 }
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
+
+// Split-key decode: the M = (H/Hkv)*Nq query rows of each key/value head (M <= 8)
+// against Nk keys cut into S ranges of `chunk` keys; partial results in opart/lpart
+// when S > 1.
+struct DecArgs {
+  const void* q;      // [B, H, Nq, d]
+  const void* k;      // [B, Hkv, Nk, d]
+  const void* v;
+  void* o;            // [B, H, Nq, d]
+  float* lse;         // [B, H, Nq]
+  float* opart;       // [S, B*Hkv, M, d] float32 (S > 1)
+  float* lpart;       // [S, B*Hkv, M] float32 natural-log lse of each range
+  int BHkv, H, Hkv, Nq, Nk, M, S, chunk, d, dtype, causal;
+  float scale_log2;
+};
+constexpr int kDecodeMaxRows = 8;
+int decode_keys_per_step(int d);
+cudaError_t launch_decode(const DecArgs& a, cudaStream_t stream);
 // Backward stages: preprocess (D, lse2, zeroed accumulator), the dK/dV kernel with
 // dQ partial sums, and the dQ conversion.
 constexpr int kBwdStagePre = 1;

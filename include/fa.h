@@ -157,6 +157,27 @@ int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const
                void* stream);
 
 /*
+ * Split-key decode: attention for a few query rows per key/value head, e.g. new
+ * tokens against a key/value cache.  Shapes, head grouping, the bottom-right causal
+ * mask and the O = 0 / lse = -inf convention are those of fa_fwd_cross; the result
+ * is the same attention (within the usual rounding).  Requires (H / Hkv) * Nq <= 8
+ * (FA_ERR_SHAPE otherwise; use fa_fwd_cross for more rows).
+ *
+ * The keys of each head are cut into ranges processed by separate CTAs on the CUDA
+ * cores (the pass reads K and V once and is bound by memory bandwidth); the
+ * per-range results are combined with lse = ln sum_s e^{lse_s},
+ * O = sum_s e^{lse_s - lse} O_s.
+ *   workspace : device scratch for the per-range results, 256-byte aligned, at least
+ *               fa_decode_workspace_size(B, H, Hkv, Nq, Nk, d) bytes (may be NULL when
+ *               that is 0); FA_ERR_WORKSPACE otherwise.  Overwritten.
+ * fa_decode_workspace_size returns 0 for invalid sizes as well.
+ */
+size_t fa_decode_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int d);
+int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
+              size_t ws_bytes, int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+              int dtype, void* stream);
+
+/*
  * The three stages fa_bwd runs, one launch each, for callers that want to time or
  * schedule them separately.  Arguments, validation and errors are exactly fa_bwd's;
  * calling the three in this order on one stream with one workspace is fa_bwd.

@@ -115,6 +115,33 @@ def test_backward_gqa_validation_codes(lib):
     assert call(ws_bytes=need - 1) == C["FA_ERR_WORKSPACE"]
 
 
+def test_decode_validation_and_workspace(lib):
+    C = binding.STATUS_CODE
+
+    def call(H=8, Hkv=2, Nq=1, Nk=4096, d=64, ws=P, ws_bytes=None, scale=0.125):
+        if ws_bytes is None:
+            ws_bytes = lib.fa_decode_workspace_size(1, H, Hkv, Nq, Nk, d)
+        return lib.fa_decode(P, P, P, P, P, ws, ws_bytes, 1, H, Hkv, Nq, Nk, d, scale, 1, 0, NULL)
+
+    assert call(Hkv=3) == C["FA_ERR_SHAPE"]
+    assert call(H=16, Hkv=1) == C["FA_ERR_SHAPE"]              # 16 rows per key/value head > 8
+    assert call(Nq=3) == C["FA_ERR_SHAPE"]                     # 4 x 3 rows > 8
+    assert call(Nk=0) == C["FA_ERR_SHAPE"]
+    assert call(d=96) == C["FA_ERR_UNSUPPORTED_D"]
+    assert call(scale=float("nan")) == C["FA_ERR_SCALE"]
+    assert call(ws=NULL) == C["FA_ERR_WORKSPACE"]
+    assert call(ws_bytes=1) == C["FA_ERR_WORKSPACE"]
+    # ranges of >= 256 keys, at most 128: per range B*Hkv*M rows of d float32 + one lse
+    for H, Hkv, Nq, Nk, d in [(8, 2, 1, 4096, 64), (4, 4, 2, 100000, 128), (32, 4, 1, 300, 64)]:
+        M = (H // Hkv) * Nq
+        smax = min(128, max(1, Nk // 256))
+        up = lambda x: (x + 255) // 256 * 256
+        expect = 0 if smax == 1 else up(smax * Hkv * M * d * 4) + up(smax * Hkv * M * 4)
+        assert lib.fa_decode_workspace_size(1, H, Hkv, Nq, Nk, d) == expect
+    assert lib.fa_decode_workspace_size(1, 8, 2, 1, 255, 64) == 0     # one range: no workspace
+    assert lib.fa_decode_workspace_size(1, 8, 3, 1, 4096, 64) == 0    # invalid grouping
+
+
 def test_backward_validation_codes(lib):
     C = binding.STATUS_CODE
     assert bwd(lib, dtype=7) == C["FA_ERR_DTYPE"]
