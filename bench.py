@@ -29,7 +29,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from exact_tiled_attention_27_gb300.inputs import WORKLOADS, workload_case  # noqa: E402
+from exact_tiled_attention_27_gb300.inputs import EXTRA_WORKLOADS, WORKLOADS, extra_case, workload_case  # noqa: E402
 
 METRIC = "attention TFLOPS fwd and fwd+bwd (bf16, causal/non) and % of GB300 BF16 tensor peak"
 UNIT = "TFLOP/s"
@@ -311,6 +311,133 @@ def run_ours(args, w, rank, world, local_rank):
     return result
 
 
+# ---------------------------------------------------------------------------- extra workloads
+def cross_visible_pairs(Nq, Nk, causal):
+    """(query row, key) pairs that take part: all of them, or under the bottom-right
+    causal mask sum_i clamp(i + Nk - Nq + 1, 0, Nk)."""
+    if not causal:
+        return Nq * Nk
+    return sum(min(Nk, max(0, i + Nk - Nq + 1)) for i in range(Nq))
+
+
+def run_extra(args, w, local_rank):
+    """Time one of the cross-length / grouped-head / decode workloads (single GPU).
+
+    cross: a step is fa_fwd_cross (+ fa_bwd_gqa when the workload has a backward);
+           TFLOP/s with 4*d (forward) and 10*d (backward) flops per visible
+           (query row, key) pair and query head.
+    decode: a step is fa_decode; GB/s of the bytes the method must move (K and V once,
+           Q, O and lse), against the measured copy bandwidth.
+    """
+    import numpy as np
+    import torch
+
+    from exact_tiled_attention_27_gb300 import build as fa_build
+    from exact_tiled_attention_27_gb300 import binding as fa
+
+    fa_build.build()
+    lib = fa.load_library()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+    sh = fa._stream_handle(stream)
+    c = extra_case(args.workload)
+    tdt = torch.bfloat16 if w["dtype"] == "bf16" else torch.float16
+    dcode = fa.FA_BF16 if w["dtype"] == "bf16" else fa.FA_FP16
+    B, H, Hkv, Nq, Nk, d = w["B"], w["H"], w["Hkv"], w["Nq"], w["Nk"], w["d"]
+    causal = 1 if w["causal"] else 0
+    up = lambda bits: torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(tdt).to(dev)  # noqa: E731
+    q, k, v = up(c.q), up(c.k), up(c.v)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
+    P = fa._ptr
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def call(st, what):
+        if st != 0:
+            raise fa.FaError(st, what)
+
+    launches = 1
+    if w["kind"] == "decode":
+        ws_bytes = int(lib.fa_decode_workspace_size(B, H, Hkv, Nq, Nk, d))
+        ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+        launches = 2 if ws_bytes > 0 else 1
+
+        def step():
+            call(lib.fa_decode(P(q), P(k), P(v), P(o), P(lse), P(ws), ws_bytes, B, H, Hkv, Nq, Nk, d, c.scale,
+                               causal, dcode, sh), "fa_decode")
+    else:
+        do = up(c.do) if w["backward"] else None
+        if w["backward"]:
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+            ws_bytes = fa.workspace_size(B, H, Nq, d)
+            ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+            launches = 4
+
+        def step():
+            call(lib.fa_fwd_cross(P(q), P(k), P(v), P(o), P(lse), B, H, Hkv, Nq, Nk, d, c.scale, causal, dcode, sh),
+                 "fa_fwd_cross")
+            if w["backward"]:
+                call(lib.fa_bwd_gqa(P(q), P(k), P(v), P(o), P(do), P(lse), P(dq), P(dk), P(dv), P(ws), ws_bytes, B,
+                                    H, Hkv, Nq, d, c.scale, causal, dcode, sh), "fa_bwd_gqa")
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.2)
+    for e0, e1 in ev:
+        flush.zero_()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    status = fa.last_kernel_status()
+    if status != 0:
+        raise RuntimeError(f"a kernel reported {fa.STATUS.get(status)} in the timed region")
+    t = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)   # ms per step
+    cfg = {"workload": f"{args.workload}: B={B} H={H} Hkv={Hkv} Nq={Nq} Nk={Nk} d={d} {w['dtype']} "
+                       f"{'causal (bottom-right)' if causal else 'non-causal'}"
+                       f"{' fwd+bwd' if w['backward'] else ''}",
+           "l2": "flushed between steps by a 256 MiB write outside the timed brackets", "parallelism": "single GPU"}
+    res = {"n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t, 5),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w["dtype"],
+           "data": "synthetic (seeded i.i.d. N(0,1) 16-bit inputs)", "config": cfg,
+           "gpu_launches": launches * args.steps}
+    if w["kind"] == "decode":
+        nbytes = 2 * B * Hkv * Nk * d * 2 + 2 * B * H * Nq * d * 2 + B * H * Nq * 4
+        gbs = nbytes / (t * 1e-3) / 1e9
+        hbm, src = 6800.0, "fallback"
+        pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
+        if os.path.exists(pk):
+            with open(pk) as f:
+                hbm, src = float(json.load(f)["hbm_gbs"]), "measured"
+        res.update({"metric": "decode: bytes of K, V, Q, O and lse moved per second", "value": round(gbs, 1),
+                    "unit": "GB/s",
+                    "roofline": {"bound": "hbm", "kernel": "decode_split_kernel", "achieved": round(gbs, 1),
+                                 "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
+                                 "peak_source": f"{src} copy bandwidth", "traffic": None}})
+    else:
+        pairs = H * B * cross_visible_pairs(Nq, Nk, bool(causal))
+        f = pairs * d * (4 + (10 if w["backward"] else 0))
+        tf = f / (t * 1e-3) / 1e12
+        peak_burst, peak_sus, src = measured_peaks()
+        res.update({"metric": "attention TFLOPS (fa_fwd_cross" + (" + fa_bwd_gqa)" if w["backward"] else ")"),
+                    "value": round(tf, 2), "unit": UNIT,
+                    "roofline": {"bound": "tensor", "kernel": "fwd_kernel" + (" + bwd_kv_kernel" if w["backward"]
+                                                                             else ""),
+                                 "achieved": round(tf, 2), "peak": peak_sus, "unit": UNIT,
+                                 "frac": round(tf / peak_sus, 4), "frac_of_burst_peak": round(tf / peak_burst, 4),
+                                 "peak_source": f"{src} bf16 cuBLAS sustained", "traffic": None}})
+    if clk:
+        res["clocks"] = clk
+    return res
+
+
 KERNEL_SOURCE = {"fwd_kernel": "fwd.cu", "bwd_kv_kernel": "bwd.cu"}
 
 
@@ -405,7 +532,7 @@ def main():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS) + sorted(EXTRA_WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="wall-clock budget of the oracle's CPU-baseline sample")
@@ -413,11 +540,15 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    w = WORKLOADS[args.workload]
-
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.workload in EXTRA_WORKLOADS:
+        if args.impl == "reference" or world > 1:
+            ap.error("the extra workloads time this library on one GPU only")
+        print(json.dumps(run_extra(args, EXTRA_WORKLOADS[args.workload], local_rank)))
+        return 0
+    w = WORKLOADS[args.workload]
 
     if args.impl == "reference":
         if rank != 0:

@@ -143,6 +143,27 @@ for _i, _n in enumerate(SWEEP_N):
             index=5, length_index=_i)
 
 
+# Workloads of the cross-length, grouped-head and decode entry points (fa_fwd_cross,
+# fa_bwd_gqa, fa_decode): prefill and chunked prefill with grouped key/value heads,
+# and decoding one new token against a key/value cache.
+EXTRA_WORKLOADS = {
+    "x1_gqa_prefill": dict(kind="cross", B=2, H=32, Hkv=8, Nq=8192, Nk=8192, d=128, dtype="bf16", causal=True,
+                           backward=True, index=20),
+    "x2_chunked_prefill": dict(kind="cross", B=4, H=32, Hkv=8, Nq=2048, Nk=16384, d=128, dtype="bf16", causal=True,
+                               backward=False, index=21),
+    "x3_decode_gqa": dict(kind="decode", B=8, H=32, Hkv=8, Nq=1, Nk=32768, d=128, dtype="bf16", causal=True,
+                          backward=False, index=22),
+    "x4_decode_mha": dict(kind="decode", B=16, H=32, Hkv=32, Nq=1, Nk=8192, d=128, dtype="bf16", causal=True,
+                          backward=False, index=23),
+}
+
+
+def extra_case(name: str) -> CrossCase:
+    w = EXTRA_WORKLOADS[name]
+    return make_cross_case(w["B"], w["H"], w["Hkv"], w["Nq"], w["Nk"], w["d"], w["dtype"], w["causal"],
+                           workload_index=w["index"], with_do=w["backward"])
+
+
 def workload_case(name: str, with_do=None) -> Case:
     w = WORKLOADS[name]
     wd = w["backward"] if with_do is None else with_do

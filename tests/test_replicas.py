@@ -50,3 +50,16 @@ def test_job_throughput_scales_with_replicas():
     assert one == pytest.approx(f / 1e-4 / 1e12)
     assert bench.job_throughput(4, f, 0.1) == pytest.approx(4 * one)
     assert bench.job_throughput(2, f, 0.2) == pytest.approx(one)   # weak scaling: slowest rank sets the pace
+
+
+def test_cross_visible_pairs_closed_forms():
+    """FLOP count of the cross-length workloads: (query, key) pairs under the
+    bottom-right causal mask."""
+    import bench
+    for n in (1, 7, 128, 1000):
+        assert bench.cross_visible_pairs(n, n, True) == n * (n + 1) // 2       # the square triangle
+        assert bench.cross_visible_pairs(n, n, False) == n * n
+    assert bench.cross_visible_pairs(1, 500, True) == 500                       # one new token sees the cache
+    assert bench.cross_visible_pairs(10, 4, True) == sum(range(1, 5))          # six rows see nothing
+    nq, nk = 300, 1000
+    assert bench.cross_visible_pairs(nq, nk, True) == nq * (nk - nq) + nq * (nq + 1) // 2
