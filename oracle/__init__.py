@@ -22,6 +22,9 @@ materialising the score matrix S and the probability matrix P on purpose:
   heads (``kv_head_of``); ``attn_gqa_bwd_ref`` -- its gradient for grouped heads.
 * ``merge_partials`` -- attention over a union of disjoint key ranges from the
   attention over each range (the split-key combine).
+* ``butterfly_mask`` / ``attn_masked_head_fwd`` / ``attn_masked_head_bwd`` -- the
+  definition with a boolean visibility mask, and the fixed butterfly block pattern of
+  block-sparse attention.
 
 Parity pins: every function here is pinned by tests in ``tests/test_oracle_pins.py``
 against printed worked examples, closed forms, invariants, library routines and
@@ -43,4 +46,8 @@ from .attention import (  # noqa: F401
     attn_gqa_bwd_ref,
     kv_head_of,
     merge_partials,
+    butterfly_pairs_visible,
+    butterfly_mask,
+    attn_masked_head_fwd,
+    attn_masked_head_bwd,
 )

@@ -33,6 +33,10 @@ __all__ = [
     "attn_gqa_bwd_ref",
     "kv_head_of",
     "merge_partials",
+    "butterfly_pairs_visible",
+    "butterfly_mask",
+    "attn_masked_head_fwd",
+    "attn_masked_head_bwd",
     "attn_rows_ref",
     "softmax_two_pass",
     "online_softmax_stats",
@@ -464,3 +468,73 @@ def merge_partials(o_parts, lse_parts):
     for s_, op in enumerate(o_parts):
         o += (w[s_] / np.where(tot > 0, tot, 1.0))[:, None] * op
     return o, lse
+
+
+# ----------------------------------------------------------------------------------
+# block-sparse attention with a fixed butterfly block pattern
+# ----------------------------------------------------------------------------------
+BUTTERFLY_BLOCK = 256
+
+
+def butterfly_pairs_visible(p, q):
+    """Block p of queries sees block q of keys in the butterfly pattern iff p == q or
+    p and q differ in exactly one bit of their block index.
+
+    [FA-review] "方法细节" names block-sparse FlashAttention with a fixed butterfly
+    mask; the pages give neither the pattern's formula nor its block size.  The
+    reading taken: the butterfly graph on block indices (an edge between indices that
+    differ in one bit, plus the diagonal), with blocks of 256 rows and keys
+    (``BUTTERFLY_BLOCK``).
+    """
+    x = int(p) ^ int(q)
+    return x == 0 or (x & (x - 1)) == 0
+
+
+def butterfly_mask(nq, nk, causal, block=BUTTERFLY_BLOCK):
+    """Boolean (nq, nk) visibility matrix: butterfly blocks, and j <= i when causal."""
+    bi = np.arange(nq)[:, None] // block
+    bj = np.arange(nk)[None, :] // block
+    x = bi ^ bj
+    vis = (x & (x - 1)) == 0
+    if causal:
+        vis &= np.arange(nk)[None, :] <= np.arange(nq)[:, None]
+    return vis
+
+
+def attn_masked_head_fwd(q, k, v, scale, mask):
+    """The definition of ``attn_head_fwd`` with an arbitrary boolean visibility mask
+    (S_ij = -inf where the mask is False).  Rows with no visible key: O = 0, LSE = -inf."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    s = np.where(mask, scale * (q @ k.T), -np.inf)
+    o = np.zeros((q.shape[0], v.shape[1]))
+    lse = np.full(q.shape[0], -np.inf)
+    live = mask.any(axis=1)
+    if live.any():
+        m = np.max(s[live], axis=1, keepdims=True)
+        e = np.exp(s[live] - m)
+        l = np.sum(e, axis=1, keepdims=True)
+        o[live] = (e / l) @ v
+        lse[live] = (m + np.log(l))[:, 0]
+    return o, lse
+
+
+def attn_masked_head_bwd(q, k, v, do, scale, mask):
+    """Gradients of sum(dO * O) for ``attn_masked_head_fwd``: (dQ, dK, dV), the
+    formulas of ``attn_head_bwd`` with P = 0 where the mask is False."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    s = np.where(mask, scale * (q @ k.T), -np.inf)
+    p = np.zeros_like(s)
+    live = mask.any(axis=1)
+    m = np.max(s[live], axis=1, keepdims=True)
+    e = np.exp(s[live] - m)
+    p[live] = e / np.sum(e, axis=1, keepdims=True)
+    dv = p.T @ do
+    dp = do @ v.T
+    d_i = np.sum(p * dp, axis=1, keepdims=True)
+    ds = p * (dp - d_i)
+    return scale * (ds @ k), scale * (ds.T @ q), dv
