@@ -20,7 +20,7 @@ FA_BF16, FA_FP16 = 0, 1
 STATUS = {
     0: "FA_OK", 1: "FA_ERR_NULL", 2: "FA_ERR_SHAPE", 3: "FA_ERR_UNSUPPORTED_D", 4: "FA_ERR_DTYPE",
     5: "FA_ERR_ALIGN", 6: "FA_ERR_WORKSPACE", 7: "FA_ERR_LAUNCH", 8: "FA_ERR_DEVICE_TIMEOUT",
-    9: "FA_ERR_NO_DEVICE", 10: "FA_ERR_SCALE", 11: "FA_ERR_SCRATCH_LIMIT",
+    9: "FA_ERR_NO_DEVICE", 10: "FA_ERR_SCALE", 11: "FA_ERR_SCRATCH_LIMIT", 12: "FA_ERR_PATTERN",
 }
 STATUS_CODE = {v: k for k, v in STATUS.items()}
 
@@ -49,6 +49,12 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
         lib.fa_fwd.restype = i
+        lib.fa_fwd_sparse.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, i, vp]
+        lib.fa_fwd_sparse.restype = i
+        lib.fa_bwd_sparse.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, f, i, i, i, vp]
+        lib.fa_bwd_sparse.restype = i
+        lib.fa_butterfly_blocks.argtypes = [i, i, i, ctypes.POINTER(ctypes.c_int), i]
+        lib.fa_butterfly_blocks.restype = i
         lib.fa_fwd_cross.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp]
         lib.fa_fwd_cross.restype = i
         lib.fa_bwd_workspace_size.argtypes = [i, i, i, i]
@@ -129,11 +135,16 @@ def workspace_size(B, H, N, d) -> int:
     return int(load_library().fa_bwd_workspace_size(B, H, N, d))
 
 
-def forward(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None):
+PATTERNS = {"butterfly": 1}
+
+
+def forward(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None, pattern=None):
     """Exact attention forward.  q, k, v: (B, H, N, d) bf16/fp16 CUDA tensors.
 
     Returns (o, lse): o like q, lse float32 (B, H, N), natural-log row log-sum-exp
     of scale * q k^T.  ``scale`` defaults to d ** -0.5.  Runs on the current stream.
+    ``pattern="butterfly"`` restricts attention to the butterfly block pattern
+    (fa_fwd_sparse).
     """
     torch = _torch()
     B, H, N, d = q.shape
@@ -148,6 +159,13 @@ def forward(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None):
     _check_bhnd("out", out, (B, H, N, d), q.dtype)
     if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous float32 (B, H, N) tensor")
+    if pattern is not None:
+        st = load_library().fa_fwd_sparse(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d, scale,
+                                          1 if causal else 0, PATTERNS[pattern], _dtype_code(q),
+                                          _stream_handle(stream))
+        if st != 0:
+            raise FaError(st, "fa_fwd_sparse")
+        return out, lse
     st = load_library().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d, scale,
                                1 if causal else 0, _dtype_code(q), _stream_handle(stream))
     if st != 0:
@@ -216,7 +234,7 @@ def decode_workspace_size(B, H, Hkv, Nq, Nk, d) -> int:
 
 
 def backward(q, k, v, o, do, lse, scale=None, causal=False, dq=None, dk=None, dv=None, workspace=None,
-             stream=None, stage=None):
+             stream=None, stage=None, pattern=None):
     """Exact attention backward.  Returns (dq, dk, dv): dq like q, dk and dv like k.
 
     k and v may have fewer heads than q (grouped key/value heads, Hkv dividing H);
@@ -251,6 +269,16 @@ def backward(q, k, v, o, do, lse, scale=None, causal=False, dq=None, dk=None, dv
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     if workspace.numel() * workspace.element_size() < need:
         raise ValueError(f"workspace too small: need {need} bytes")
+    if pattern is not None:
+        if Hkv != H or stage is not None:
+            raise ValueError("the block pattern takes Hkv == H and the whole backward")
+        st = load_library().fa_bwd_sparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                                          _ptr(dk), _ptr(dv), _ptr(workspace), need, B, H, N, d, scale,
+                                          1 if causal else 0, PATTERNS[pattern], _dtype_code(q),
+                                          _stream_handle(stream))
+        if st != 0:
+            raise FaError(st, "fa_bwd_sparse")
+        return dq, dk, dv
     if Hkv != H:
         fn_name = "fa_bwd_gqa"
         st = load_library().fa_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),

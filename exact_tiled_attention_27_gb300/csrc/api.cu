@@ -161,7 +161,7 @@ using namespace fa;
 extern "C" {
 
 static int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv,
-                      int Nq, int Nk, int d, float scale, int causal, int dtype, void* stream) {
+                      int Nq, int Nk, int d, float scale, int causal, int dtype, void* stream, int pattern = 0) {
   int st = check_common(B, H, Nq, d, scale, dtype);
   if (st != FA_OK) return st;
   if (Hkv < 1 || Hkv > H || H % Hkv != 0) return FA_ERR_SHAPE;
@@ -192,6 +192,7 @@ static int fwd_common(const void* q, const void* k, const void* v, void* o, floa
   a.err_word = dev->err_word;
   a.limit_ns = kWaitLimitNs;
   a.num_sms = dev->num_sms;
+  a.pattern = pattern;
   return launch_fwd(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
@@ -205,6 +206,20 @@ int fa_fwd_cross(const void* q, const void* k, const void* v, void* o, float* ls
   return fwd_common(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, scale, causal, dtype, stream);
 }
 
+int fa_fwd_sparse(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                  float scale, int causal, int pattern, int dtype, void* stream) {
+  if (pattern != FA_PATTERN_BUTTERFLY) return FA_ERR_PATTERN;
+  return fwd_common(q, k, v, o, lse, B, H, H, N, N, d, scale, causal, dtype, stream, 1);
+}
+
+int fa_butterfly_blocks(int nblocks, int pair, int causal_dir, int* out, int cap) {
+  const int npairs = (nblocks + 1) / 2;
+  if (nblocks < 1 || pair < 0 || pair >= npairs || causal_dir < -1 || causal_dir > 1) return -1;
+  const int n = bfly_blocks(pair, npairs, nblocks, causal_dir, 0);
+  for (int j = 0; j < n && j < cap; ++j) out[j] = bfly_block(pair, j, npairs, causal_dir, 0);
+  return n;
+}
+
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   if (check_common(B, H, N, d, 1.0f, FA_BF16) != FA_OK) return 0;
   return ws_layout(B, H, N, d).total;
@@ -212,7 +227,7 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
 
 static int bwd_common(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                       void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes, int B, int H, int Hkv, int N,
-                      int d, float scale, int causal, int dtype, void* stream, int stages) {
+                      int d, float scale, int causal, int dtype, void* stream, int stages, int pattern = 0) {
   int st = check_common(B, H, N, d, scale, dtype);
   if (st != FA_OK) return st;
   if (Hkv < 1 || Hkv > H || H % Hkv != 0) return FA_ERR_SHAPE;
@@ -260,6 +275,7 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
   // every key block re-reads the Q and dO (16-bit) of the key/value head's G query heads
   // and adds into their float32 dQ
   a.heads_per_group = heads_per_group(8LL * a.G * N * d, dev->l2_bytes, a.BHkv);
+  a.pattern = pattern;
   return launch_bwd(a, static_cast<cudaStream_t>(stream), stages) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
@@ -369,6 +385,14 @@ int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, 
   return launch_decode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
+int fa_bwd_sparse(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                  void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes, int B, int H, int N, int d,
+                  float scale, int causal, int pattern, int dtype, void* stream) {
+  if (pattern != FA_PATTERN_BUTTERFLY) return FA_ERR_PATTERN;
+  return bwd_common(q, k, v, o, dO, lse, dq, dk, dv, workspace, ws_bytes, B, H, H, N, d, scale, causal, dtype,
+                    stream, kBwdStagePre | kBwdStageKV | kBwdStageDQ, 1);
+}
+
 const char* fa_strerror(int status) {
   switch (status) {
     case FA_OK: return "ok";
@@ -382,6 +406,7 @@ const char* fa_strerror(int status) {
     case FA_ERR_DEVICE_TIMEOUT: return "a kernel's bounded pipeline wait gave up";
     case FA_ERR_NO_DEVICE: return "no usable sm_100-family CUDA device is current";
     case FA_ERR_SCALE: return "scale must be finite and > 0";
+    case FA_ERR_PATTERN: return "unknown block pattern (FA_PATTERN_BUTTERFLY is the only one)";
     case FA_ERR_SCRATCH_LIMIT:
       return "fa_bwd_noalloc: these sizes need more scratch than its built-in array (fa_bwd_noalloc_max_scratch)";
     default: return "unknown status";

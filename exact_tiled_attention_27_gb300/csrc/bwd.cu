@@ -108,9 +108,10 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int u) {
   return static_cast<uint32_t>(r * 128 + ((u ^ (r & 7)) << 4));
 }
 
-// GQA: key/value heads shared by groups of G > 1 query heads (fa_bwd_gqa); otherwise
-// G = 1 and the query head is the key/value head.
-template <int D, int DT, bool CAUSAL, bool GQA>
+// MODE 1 (GQA): key/value heads shared by groups of G > 1 query heads (fa_bwd_gqa).
+// MODE 2 (SPARSE): the butterfly block pattern (fa_bwd_sparse): a key block visits the
+// query blocks of its pair's linked pairs.  MODE 0: G = 1, dense.
+template <int D, int DT, bool CAUSAL, int MODE>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -136,8 +137,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // The query heads that read key/value head bhk are G consecutive heads starting at
   // first_q_head(bhk); a tile's steps run over all of their query blocks, so dK and dV
   // sum over the group in tensor memory.  G = 1 is ordinary multi-head attention.
+  constexpr bool GQA = MODE == 1;
+  constexpr bool SPARSE = MODE == 2;
   auto first_q_head = [&](int bhk) { return GQA ? (bhk / (H / G)) * H + (bhk % (H / G)) * G : bhk; };
   const int group = GQA ? G : 1;
+  // butterfly lists of a key block: its pair, upward under the causal mask, without the
+  // even query block of its own pair when the key block is odd (that block lies above
+  // the diagonal)
+  const int npairs = (nb + 1) >> 1;
+  constexpr int kDir = CAUSAL ? 1 : 0;
+  auto skip_of = [&](int kb) { return (CAUSAL && (kb & 1)) ? 1 : 0; };
+  auto sparse_q = [&](int kb, int j) { return bfly_block(kb >> 1, j, npairs, kDir, skip_of(kb)); };
+  auto sparse_n = [&](int kb) { return bfly_blocks(kb >> 1, npairs, nb, kDir, skip_of(kb)); };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kKVBufs; ++i) {
@@ -238,10 +249,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
         }
         __syncwarp();
-        const int q0 = CAUSAL ? kb : 0;
+        const int q0 = SPARSE ? sparse_q(kb, 0) : (CAUSAL ? kb : 0);
+        const int nq = SPARSE ? sparse_n(kb) : 0;
         for (int g = 0; ok && g < group; ++g) {
         const int bhq = first_q_head(bh) + g;
-        for (int qi = q0; qi < nb; ++qi, ++s) {
+        for (int qi = q0, j = 0; SPARSE ? j < nq : qi < nb; ++s, ++j, qi = SPARSE ? sparse_q(kb, j) : qi + 1) {
           const int qs = s % C::kQBufs;
           if (s >= (uint32_t)C::kQBufs && !wait_warp(bar(C::kQEmpty + qs), ((s / C::kQBufs) - 1) & 1, ctl, 0x402)) {
             ok = false;
@@ -324,7 +336,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         group_order(tile, BHkv, nb, hg, kb, bh);
         const int kvb = it % C::kKVBufs;
         const int q0 = CAUSAL ? kb : 0;
-        const int nsteps = group * (nb - q0);
+        const int nsteps = SPARSE ? sparse_n(kb) : group * (nb - q0);
         if (!wait_warp(bar(C::kKVFull + kvb), (it / C::kKVBufs) & 1, ctl, 0x501)) break;
         const uint32_t kbase = smem_u32(smem + C::kOffK + kvb * C::kTileBytes);
         const uint32_t vbase = smem_u32(smem + C::kOffV + kvb * C::kTileBytes);
@@ -445,10 +457,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (tile < 0) break;
       int kb, bh;
       group_order(tile, BHkv, nb, hg, kb, bh);
-      const int q0 = CAUSAL ? kb : 0;
+      const int q0 = SPARSE ? sparse_q(kb, 0) : (CAUSAL ? kb : 0);
+      const int nq = SPARSE ? sparse_n(kb) : 0;
       bool ok = true;
       for (int g = 0; ok && g < group; ++g)
-      for (int qi = q0; qi < nb; ++qi, ++s) {
+      for (int qi = q0, j = 0; SPARSE ? j < nq : qi < nb; ++s, ++j, qi = SPARSE ? sparse_q(kb, j) : qi + 1) {
         const int qs = s % C::kQBufs;
         bool w = mbar_wait(bar(C::kSFull), s & 1, ctl, 0x601);
         w = w && mbar_wait(bar(C::kQFull + qs), (s / C::kQBufs) & 1, ctl, 0x602);
@@ -560,11 +573,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (tile < 0) break;
       int kb, bh;
       group_order(tile, BHkv, nb, hg, kb, bh);
-      const int q0 = CAUSAL ? kb : 0;
+      const int q0 = SPARSE ? sparse_q(kb, 0) : (CAUSAL ? kb : 0);
+      const int nq = SPARSE ? sparse_n(kb) : 0;
       bool ok = true;
       for (int g = 0; ok && g < group; ++g) {
       const int bhq = first_q_head(bh) + g;
-      for (int qi = q0; qi < nb; ++qi, ++s) {
+      for (int qi = q0, j = 0; SPARSE ? j < nq : qi < nb; ++s, ++j, qi = SPARSE ? sparse_q(kb, j) : qi + 1) {
         if (!wait_warp(bar(C::kDQFull), s & 1, ctl, 0x701)) {
           ok = false;
           break;
@@ -572,7 +586,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // d = 64: the next tile's first gradient MMAs wait for the dK/dV columns, so
         // those are read out before the last dQ of the tile (at d = 128 the next
         // tile's first scores wait for the dQ columns instead, so dQ goes first)
-        if (C::kEarly && g == group - 1 && qi == nb - 1 && !write_dkdv(it, kb, bh)) {
+        if (C::kEarly && g == group - 1 && (SPARSE ? j == nq - 1 : qi == nb - 1) && !write_dkdv(it, kb, bh)) {
           ok = false;
           break;
         }
@@ -697,7 +711,7 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ a
   }
 }
 
-template <int D, int DT, bool CAUSAL, bool GQA>
+template <int D, int DT, bool CAUSAL, int MODE>
 cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int stages) {
   using C = BwdCfg<D>;
   if (stages & kBwdStagePre) {
@@ -713,7 +727,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int stages) {
     if (e != cudaSuccess) return e;
   }
   if (stages & kBwdStageKV) {
-    auto kern = bwd_kv_kernel<D, DT, CAUSAL, GQA>;
+    auto kern = bwd_kv_kernel<D, DT, CAUSAL, MODE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     // the setmaxnreg split inside the kernel must fit what the launch provides
@@ -741,25 +755,26 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int stages) {
   return cudaSuccess;
 }
 
-template <bool GQA>
+template <int MODE>
 cudaError_t launch_bwd_g(const BwdArgs& a, cudaStream_t stream, int stages) {
   const int key = (a.d == 128 ? 4 : 0) | (a.dtype == 1 ? 2 : 0) | (a.causal ? 1 : 0);
   switch (key) {
-    case 0: return launch_bwd_t<64, 0, false, GQA>(a, stream, stages);
-    case 1: return launch_bwd_t<64, 0, true, GQA>(a, stream, stages);
-    case 2: return launch_bwd_t<64, 1, false, GQA>(a, stream, stages);
-    case 3: return launch_bwd_t<64, 1, true, GQA>(a, stream, stages);
-    case 4: return launch_bwd_t<128, 0, false, GQA>(a, stream, stages);
-    case 5: return launch_bwd_t<128, 0, true, GQA>(a, stream, stages);
-    case 6: return launch_bwd_t<128, 1, false, GQA>(a, stream, stages);
-    default: return launch_bwd_t<128, 1, true, GQA>(a, stream, stages);
+    case 0: return launch_bwd_t<64, 0, false, MODE>(a, stream, stages);
+    case 1: return launch_bwd_t<64, 0, true, MODE>(a, stream, stages);
+    case 2: return launch_bwd_t<64, 1, false, MODE>(a, stream, stages);
+    case 3: return launch_bwd_t<64, 1, true, MODE>(a, stream, stages);
+    case 4: return launch_bwd_t<128, 0, false, MODE>(a, stream, stages);
+    case 5: return launch_bwd_t<128, 0, true, MODE>(a, stream, stages);
+    case 6: return launch_bwd_t<128, 1, false, MODE>(a, stream, stages);
+    default: return launch_bwd_t<128, 1, true, MODE>(a, stream, stages);
   }
 }
 
 }  // namespace
 
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream, int stages) {
-  return a.G != 1 ? launch_bwd_g<true>(a, stream, stages) : launch_bwd_g<false>(a, stream, stages);
+  if (a.pattern == 1) return launch_bwd_g<2>(a, stream, stages);
+  return a.G != 1 ? launch_bwd_g<1>(a, stream, stages) : launch_bwd_g<0>(a, stream, stages);
 }
 
 }  // namespace fa

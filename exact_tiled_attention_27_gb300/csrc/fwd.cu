@@ -127,7 +127,9 @@ __host__ __device__ __forceinline__ int visible_kv_blocks(int qb, int Nq, int Nk
 //             numbered heaviest first under the causal mask.
 //   balanced  (i, nqb-1-i): under the causal mask every pair costs nqb+1 blocks, which
 //             evens out the work when there are only about as many pairs as SMs.
-template <bool GEN>
+// MODE: 0 plain (Nq = Nk, one key/value head per query head), 1 general (fa_fwd_cross),
+// 2 butterfly block pattern (fa_fwd_sparse).
+template <int MODE>
 __device__ __forceinline__ TileInfo decode_tile(int tile, int BH, int H, int G, int Nq, int Nk, bool causal,
                                                 bool balanced) {
   const int nqb = (Nq + kTileRows - 1) / kTileRows;
@@ -135,7 +137,7 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, int BH, int H, int G, 
   TileInfo ti;
   const int r = tile / BH;
   ti.bh = tile - r * BH;
-  ti.kvh = GEN ? (ti.bh / H) * (H / G) + (ti.bh % H) / G : ti.bh;
+  ti.kvh = MODE == 1 ? (ti.bh / H) * (H / G) + (ti.bh % H) / G : ti.bh;
   if (balanced) {
     ti.qb0 = r;
     ti.qb1 = nqb - 1 - r;
@@ -144,9 +146,15 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, int BH, int H, int G, 
     ti.qb1 = ti.qb0 + 1;
   }
   ti.has1 = ti.qb1 < nqb && ti.qb1 != ti.qb0;
-  if constexpr (GEN) {
+  if constexpr (MODE == 1) {
     ti.n0 = visible_kv_blocks(ti.qb0, Nq, Nk, causal);
     ti.n1 = ti.has1 ? visible_kv_blocks(ti.qb1, Nq, Nk, causal) : 0;
+  } else if constexpr (MODE == 2) {
+    // both query blocks of pair p = qb0/2 walk the key blocks of p's linked pairs; under
+    // the causal mask the list ends with block qb1, which query block qb0 does not see
+    const int n = bfly_blocks(ti.qb0 >> 1, npairs, nqb, causal ? -1 : 0, 0);
+    ti.n1 = ti.has1 ? n : 0;
+    ti.n0 = (causal && ti.has1) ? n - 1 : n;
   } else {   // Nq = Nk: block qb sees blocks 0..qb under the causal mask
     ti.n0 = causal ? ti.qb0 + 1 : nqb;
     ti.n1 = ti.has1 ? (causal ? ti.qb1 + 1 : nqb) : 0;
@@ -155,15 +163,18 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, int BH, int H, int G, 
   return ti;
 }
 
-// GEN: Nq != Nk or grouped key/value heads (fa_fwd_cross); otherwise Nq = Nk and every
-// query head has its own key/value head, and rows always see at least one key.
-template <int D, int DT, bool CAUSAL, bool GEN>
+// MODE 1 (GEN): Nq != Nk or grouped key/value heads (fa_fwd_cross).  MODE 2 (SPARSE):
+// the butterfly block pattern (fa_fwd_sparse).  MODE 0: Nq = Nk, every query head has
+// its own key/value head, and rows always see at least one key.
+template <int D, int DT, bool CAUSAL, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, uint16_t* __restrict__ out, float* __restrict__ lse,
                int BH, int H, int G, int Nq, int Nk, float scale_log2, int balanced, unsigned int* err_word,
                uint64_t limit_ns) {
   using C = FwdCfg<D>;
+  constexpr bool GEN = MODE == 1;
+  constexpr bool SPARSE = MODE == 2;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned base, derived from the __shared__ array by pointer arithmetic so
   // that every access through it stays a shared-memory access (not a generic one)
@@ -178,6 +189,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = __shfl_sync(0xffffffffu, threadIdx.x >> 5, 0);
   const int nqb = (Nq + kTileRows - 1) / kTileRows;
   const int ntiles = BH * ((nqb + 1) >> 1);
+  // key block of step j of tile ti: j, or the j-th block of the pair's butterfly list
+  auto key_block = [&](const TileInfo& ti, int j) {
+    return SPARSE ? bfly_block(ti.qb0 >> 1, j, (nqb + 1) >> 1, CAUSAL ? -1 : 0, 0) : j;
+  };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kQBufs; ++i) {
@@ -235,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0;
       bool ok = true;
       for (int k = 0, tile = persistent_tile(0); ok && tile < ntiles; tile = persistent_tile(++k), ++it) {
-        const TileInfo ti = decode_tile<GEN>(tile, BH, H, G, Nq, Nk, CAUSAL, balanced != 0);
+        const TileInfo ti = decode_tile<MODE>(tile, BH, H, G, Nq, Nk, CAUSAL, balanced != 0);
         const int qbuf = it % C::kQBufs;
         if (it >= C::kQBufs && !wait_warp(bar(C::kQEmpty + qbuf), ((it / C::kQBufs) - 1) & 1, ctl, 0x101)) {
           ok = false;
@@ -267,11 +282,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(bar(C::kKFull + st), C::kTileBytes);
 #pragma unroll
             for (int c = 0; c < C::kChunks; ++c)
-              tma_load_3d(kdst + c * kChunkBytes, &tm_k, bar(C::kKFull + st), c * 64, j * kTileRows, ti.kvh);
+              tma_load_3d(kdst + c * kChunkBytes, &tm_k, bar(C::kKFull + st), c * 64, key_block(ti, j) * kTileRows,
+                          ti.kvh);
             mbar_arrive_expect_tx(bar(C::kVFull + st), C::kTileBytes);
 #pragma unroll
             for (int c = 0; c < C::kChunks; ++c)
-              tma_load_3d(vdst + c * kChunkBytes, &tm_v, bar(C::kVFull + st), c * 64, j * kTileRows, ti.kvh);
+              tma_load_3d(vdst + c * kChunkBytes, &tm_v, bar(C::kVFull + st), c * 64, key_block(ti, j) * kTileRows,
+                          ti.kvh);
           }
           __syncwarp();
         }
@@ -315,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       for (int k = 0, tile = persistent_tile(0); ok && tile < ntiles; tile = persistent_tile(++k), ++it) {
-        const TileInfo ti = decode_tile<GEN>(tile, BH, H, G, Nq, Nk, CAUSAL, balanced != 0);
+        const TileInfo ti = decode_tile<MODE>(tile, BH, H, G, Nq, Nk, CAUSAL, balanced != 0);
         const int n[2] = {ti.n0, ti.n1};
         const int qbuf = it % C::kQBufs;
         const uint32_t qbase0 = smem_u32(smem + C::kOffQ + (qbuf * 2) * C::kTileBytes);
@@ -407,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t c = 0;   // steps of this sub-tile (S-full / P-full phases)
     uint32_t e = 0;   // epilogues of this sub-tile
     for (int k = 0, tile = persistent_tile(0); tile < ntiles; tile = persistent_tile(++k)) {
-      const TileInfo ti = decode_tile<GEN>(tile, BH, H, G, Nq, Nk, CAUSAL, balanced != 0);
+      const TileInfo ti = decode_tile<MODE>(tile, BH, H, G, Nq, Nk, CAUSAL, balanced != 0);
       const int n = t == 0 ? ti.n0 : ti.n1;
       const int qb = t == 0 ? ti.qb0 : ti.qb1;
       const int row = qb * kTileRows + tid;
@@ -442,8 +459,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
         reg_fence<128>(sr);
         float* s = reinterpret_cast<float*>(sr);
-        const int kbase = j * kTileRows;
-        if (GEN ? (kbase + kTileRows - 1 > lim_blk) : ((kbase + kTileRows > Nk) || (CAUSAL && j == qb))) {
+        const int kb = key_block(ti, j);
+        const int kbase = kb * kTileRows;
+        if (GEN ? (kbase + kTileRows - 1 > lim_blk) : ((kbase + kTileRows > Nk) || (CAUSAL && kb == qb))) {
 #pragma unroll
           for (int q = 0; q < 128; ++q)
             if (kbase + q > lim_row) s[q] = -INFINITY;
@@ -595,10 +613,10 @@ int choose_balanced_pairing(int BH, int Nq, int Nk, int grid) {
   return worst[1] < worst[0] ? 1 : 0;
 }
 
-template <int D, int DT, bool CAUSAL, bool GEN>
+template <int D, int DT, bool CAUSAL, int MODE>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   using C = FwdCfg<D>;
-  auto kern = fwd_kernel<D, DT, CAUSAL, GEN>;
+  auto kern = fwd_kernel<D, DT, CAUSAL, MODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   // The register split inside the kernel must fit what the launch provides, or the
@@ -610,31 +628,33 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   const int nqb = (a.Nq + kTileRows - 1) / kTileRows;
   const int ntiles = a.BH * ((nqb + 1) / 2);
   const int grid = ntiles < a.num_sms ? ntiles : a.num_sms;
-  const int balanced = CAUSAL ? choose_balanced_pairing(a.BH, a.Nq, a.Nk, grid) : 0;
+  // (the butterfly pattern is defined on adjacent pairs of query blocks)
+  const int balanced = (CAUSAL && MODE != 2) ? choose_balanced_pairing(a.BH, a.Nq, a.Nk, grid) : 0;
   return launch_overlapped(kern, grid, kThreads, C::kSmemBytes, stream, a.tm_q, a.tm_k, a.tm_v,
                            static_cast<uint16_t*>(a.o), a.lse, a.BH, a.H, a.G, a.Nq, a.Nk, a.scale_log2, balanced,
                            a.err_word, a.limit_ns);
 }
 
-template <bool GEN>
+template <int MODE>
 cudaError_t launch_fwd_g(const FwdArgs& a, cudaStream_t stream) {
   const int key = (a.d == 128 ? 4 : 0) | (a.dtype == 1 ? 2 : 0) | (a.causal ? 1 : 0);
   switch (key) {
-    case 0: return launch_fwd_t<64, 0, false, GEN>(a, stream);
-    case 1: return launch_fwd_t<64, 0, true, GEN>(a, stream);
-    case 2: return launch_fwd_t<64, 1, false, GEN>(a, stream);
-    case 3: return launch_fwd_t<64, 1, true, GEN>(a, stream);
-    case 4: return launch_fwd_t<128, 0, false, GEN>(a, stream);
-    case 5: return launch_fwd_t<128, 0, true, GEN>(a, stream);
-    case 6: return launch_fwd_t<128, 1, false, GEN>(a, stream);
-    default: return launch_fwd_t<128, 1, true, GEN>(a, stream);
+    case 0: return launch_fwd_t<64, 0, false, MODE>(a, stream);
+    case 1: return launch_fwd_t<64, 0, true, MODE>(a, stream);
+    case 2: return launch_fwd_t<64, 1, false, MODE>(a, stream);
+    case 3: return launch_fwd_t<64, 1, true, MODE>(a, stream);
+    case 4: return launch_fwd_t<128, 0, false, MODE>(a, stream);
+    case 5: return launch_fwd_t<128, 0, true, MODE>(a, stream);
+    case 6: return launch_fwd_t<128, 1, false, MODE>(a, stream);
+    default: return launch_fwd_t<128, 1, true, MODE>(a, stream);
   }
 }
 
 }  // namespace
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
-  return (a.Nq != a.Nk || a.G != 1) ? launch_fwd_g<true>(a, stream) : launch_fwd_g<false>(a, stream);
+  if (a.pattern == 1) return launch_fwd_g<2>(a, stream);
+  return (a.Nq != a.Nk || a.G != 1) ? launch_fwd_g<1>(a, stream) : launch_fwd_g<0>(a, stream);
 }
 
 }  // namespace fa

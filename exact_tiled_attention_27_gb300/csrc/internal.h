@@ -20,6 +20,7 @@ struct FwdArgs {
   void* o;
   float* lse;
   int BH, H, G, Nq, Nk, d, dtype, causal;   // G = query heads per key/value head
+  int pattern;                   // 0 dense, 1 butterfly block pattern (Nq = Nk, G = 1)
   float scale_log2;              // scale * log2(e)
   unsigned int* err_word;
   uint64_t limit_ns;
@@ -42,6 +43,7 @@ struct BwdArgs {
   unsigned int* tile_counter;  // tiles handed out beyond the first one per CTA
   int BH, N, Npad, d, dtype, causal;   // BH = B*H query heads
   int BHkv, H, G;                      // B*Hkv key/value heads; G = H / Hkv query heads per key/value head
+  int pattern;                         // 0 dense, 1 butterfly block pattern (G = 1)
   float scale, scale_log2;
   unsigned int* err_word;
   uint64_t limit_ns;
@@ -61,6 +63,60 @@ __host__ __device__ __forceinline__ void group_order(int tile, int BH, int units
   const int gh = (BH - grp * hg) < hg ? (BH - grp * hg) : hg;
   r = within / gh;
   bh = grp * hg + (within - r * gh);
+}
+
+// ---------------------------------------------------------------- butterfly block pattern
+// Block-sparse attention with a fixed butterfly pattern on blocks of 256 rows / keys
+// (pairs of 128-row tiles): pair p and pair q are linked iff p == q or p ^ q has exactly
+// one bit set.  dir < 0 keeps only pairs <= p (causal forward: keys of a query pair),
+// dir > 0 only pairs >= p (causal backward: queries of a key pair), dir == 0 all.
+// Linked pairs in increasing order: p with one set bit cleared (highest bit first),
+// p itself, p with one clear bit set (lowest bit first) while below npairs.
+__host__ __device__ inline int bfly_count(int p, int npairs, int dir) {
+  int n = 1;
+  for (int b = 0; b < 31 && (1 << b) <= (p > npairs ? p : npairs); ++b) {
+    const int c = p ^ (1 << b);
+    if (c < p ? dir <= 0 : (dir >= 0 && c < npairs)) ++n;
+  }
+  return n;
+}
+
+__host__ __device__ inline int bfly_pair(int p, int i, int npairs, int dir) {
+  if (dir <= 0) {
+    for (int b = 30; b >= 0; --b)
+      if ((p >> b) & 1) {
+        if (i == 0) return p ^ (1 << b);
+        --i;
+      }
+  }
+  if (i == 0) return p;
+  --i;
+  for (int b = 0; b < 31 && (1 << b) < npairs; ++b)
+    if (!((p >> b) & 1)) {
+      const int c = p | (1 << b);
+      if (c < npairs) {
+        if (i == 0) return c;
+        --i;
+      }
+    }
+  return -1;
+}
+
+// The 128-row blocks of the linked pairs, in order: block j is half (j + skip) & 1 of
+// linked pair (j + skip) >> 1.  skip = 1 drops the first block (the causal backward of an
+// odd key block does not see the even query block of its own pair).  With an odd
+// number of blocks the last pair holds one block; it is the largest pair, so when
+// linked it is the last in the list and only the count changes.
+__host__ __device__ inline int bfly_block(int p, int j, int npairs, int dir, int skip) {
+  const int jj = j + skip;
+  return 2 * bfly_pair(p, jj >> 1, npairs, dir) + (jj & 1);
+}
+
+__host__ __device__ inline int bfly_blocks(int p, int npairs, int nblocks, int dir, int skip) {
+  const int cnt = bfly_count(p, npairs, dir);
+  int n = 2 * cnt - skip;
+  if ((nblocks & 1) && bfly_pair(p, cnt - 1, npairs, dir) == npairs - 1) --n;
+  return n;
 }
 
 // Heads per group so that `bytes_per_head` of re-read data for one group fits in

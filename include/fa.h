@@ -63,9 +63,13 @@ typedef enum {
   FA_ERR_DEVICE_TIMEOUT = 8,  /* a kernel's bounded pipeline wait gave up          */
   FA_ERR_NO_DEVICE = 9,       /* no usable sm_100-family device is current         */
   FA_ERR_SCALE = 10,          /* scale not finite or not > 0                       */
-  FA_ERR_SCRATCH_LIMIT = 11   /* fa_bwd_noalloc: the problem needs more scratch than
+  FA_ERR_SCRATCH_LIMIT = 11,  /* fa_bwd_noalloc: the problem needs more scratch than
                                  the library's built-in array holds                 */
+  FA_ERR_PATTERN = 12         /* fa_fwd_sparse / fa_bwd_sparse: unknown block pattern */
 } fa_status;
+
+/* Block patterns of fa_fwd_sparse / fa_bwd_sparse. */
+typedef enum { FA_PATTERN_BUTTERFLY = 1 } fa_pattern;
 
 /*
  * Forward: O and lse from Q, K, V.
@@ -176,6 +180,34 @@ size_t fa_decode_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int d);
 int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
               size_t ws_bytes, int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int causal,
               int dtype, void* stream);
+
+/*
+ * Block-sparse attention with a fixed butterfly pattern (FlashAttention review,
+ * "方法细节": block-sparse FlashAttention with a fixed butterfly mask).  The pattern's
+ * blocks are 256 rows and 256 keys (two 128-row tiles): query block p sees key block q
+ * iff p == q or the binary block indices differ in exactly one bit.  With `causal` the
+ * element mask key <= query applies on top.  Blocks outside the pattern are never
+ * loaded or computed (as the causal skip), so the work grows as N log N.
+ *   pattern : FA_PATTERN_BUTTERFLY (FA_ERR_PATTERN otherwise).
+ * Shapes, layout, dtypes, lse, workspace and errors are those of fa_fwd / fa_bwd
+ * (square N, one key/value head per query head).
+ */
+int fa_fwd_sparse(const void* q, const void* k, const void* v, void* o, float* lse,
+                  int B, int H, int N, int d, float scale, int causal, int pattern, int dtype,
+                  void* stream);
+int fa_bwd_sparse(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                  const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+                  int B, int H, int N, int d, float scale, int causal, int pattern, int dtype,
+                  void* stream);
+
+/*
+ * Host utility: the 128-row key blocks that the query blocks of butterfly pair `pair`
+ * (query blocks 2*pair and 2*pair+1) visit, in order, for `nblocks` 128-row blocks.
+ * causal_dir: 0 all linked pairs, -1 only pairs <= `pair` (the causal forward), +1 only
+ * pairs >= `pair`.  Writes up to `cap` block indices to `out` and returns their number
+ * (-1 for invalid arguments).  Runs on the host; needs no device.
+ */
+int fa_butterfly_blocks(int nblocks, int pair, int causal_dir, int* out, int cap);
 
 /*
  * The three stages fa_bwd runs, one launch each, for callers that want to time or

@@ -142,6 +142,36 @@ def test_decode_validation_and_workspace(lib):
     assert lib.fa_decode_workspace_size(1, 8, 3, 1, 4096, 64) == 0    # invalid grouping
 
 
+def test_butterfly_blocks_match_brute_force(lib):
+    """The key blocks each butterfly query pair visits (host utility of the library)."""
+    buf = (ctypes.c_int * 64)()
+    for nblocks in (1, 2, 3, 7, 8, 16, 33, 64):
+        npairs = (nblocks + 1) // 2
+        for pair in range(npairs):
+            for direction in (-1, 0, 1):
+                want = []
+                for p2 in range(npairs):
+                    x = pair ^ p2
+                    if (x & (x - 1)) == 0 and (direction == 0 or (p2 <= pair if direction < 0 else p2 >= pair)):
+                        want += [b for b in (2 * p2, 2 * p2 + 1) if b < nblocks]
+                n = lib.fa_butterfly_blocks(nblocks, pair, direction, buf, 64)
+                assert n == len(want) and list(buf[:n]) == want, (nblocks, pair, direction)
+    assert lib.fa_butterfly_blocks(0, 0, 0, buf, 64) == -1
+    assert lib.fa_butterfly_blocks(8, 4, 0, buf, 64) == -1     # pair out of range
+    assert lib.fa_butterfly_blocks(8, 0, 2, buf, 64) == -1
+
+
+def test_sparse_validation_codes(lib):
+    C = binding.STATUS_CODE
+    assert lib.fa_fwd_sparse(P, P, P, P, P, 1, 1, 512, 64, 0.125, 0, 2, 0, NULL) == C["FA_ERR_PATTERN"]
+    assert lib.fa_fwd_sparse(P, P, P, P, P, 1, 1, 0, 64, 0.125, 0, 1, 0, NULL) == C["FA_ERR_SHAPE"]
+    need = lib.fa_bwd_workspace_size(1, 1, 512, 64)
+    assert lib.fa_bwd_sparse(P, P, P, P, P, P, P, P, P, P, need, 1, 1, 512, 64, 0.125, 0, 0, 0, NULL) == \
+        C["FA_ERR_PATTERN"]
+    assert lib.fa_bwd_sparse(P, P, P, P, P, P, P, P, P, NULL, need, 1, 1, 512, 64, 0.125, 0, 1, 0, NULL) == \
+        C["FA_ERR_WORKSPACE"]
+
+
 def test_backward_validation_codes(lib):
     C = binding.STATUS_CODE
     assert bwd(lib, dtype=7) == C["FA_ERR_DTYPE"]
