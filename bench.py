@@ -320,6 +320,27 @@ def cross_visible_pairs(Nq, Nk, causal):
     return sum(min(Nk, max(0, i + Nk - Nq + 1)) for i in range(Nq))
 
 
+def butterfly_visible_pairs(N, causal, block=128):
+    """(query row, key) pairs inside the butterfly pattern (256-row blocks = pairs of
+    128-row tiles linked when equal or one bit apart), with key <= query when causal."""
+    nb = (N + block - 1) // block
+    npairs = (nb + 1) // 2
+    total = 0
+    for i in range(nb):
+        rows = min(N, (i + 1) * block) - i * block
+        for kb in range(nb):
+            x = (i // 2) ^ (kb // 2)
+            if kb // 2 >= npairs or (x & (x - 1)) != 0:
+                continue
+            k0, k1 = kb * block, min(N, (kb + 1) * block)
+            if not causal:
+                total += rows * (k1 - k0)
+            else:
+                for r in range(i * block, i * block + rows):
+                    total += max(0, min(k1, r + 1) - k0)
+    return total
+
+
 def run_extra(args, w, local_rank):
     """Time one of the cross-length / grouped-head / decode workloads (single GPU).
 
@@ -358,7 +379,25 @@ def run_extra(args, w, local_rank):
             raise fa.FaError(st, what)
 
     launches = 1
-    if w["kind"] == "decode":
+    dense_step = None
+    if w["kind"] == "sparse":
+        do = up(c.do)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws_bytes = fa.workspace_size(B, H, Nq, d)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        launches = 4
+
+        def step():
+            call(lib.fa_fwd_sparse(P(q), P(k), P(v), P(o), P(lse), B, H, Nq, d, c.scale, causal, 1, dcode, sh),
+                 "fa_fwd_sparse")
+            call(lib.fa_bwd_sparse(P(q), P(k), P(v), P(o), P(do), P(lse), P(dq), P(dk), P(dv), P(ws), ws_bytes, B, H,
+                                   Nq, d, c.scale, causal, 1, dcode, sh), "fa_bwd_sparse")
+
+        def dense_step():
+            call(lib.fa_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, Nq, d, c.scale, causal, dcode, sh), "fa_fwd")
+            call(lib.fa_bwd(P(q), P(k), P(v), P(o), P(do), P(lse), P(dq), P(dk), P(dv), P(ws), ws_bytes, B, H, Nq, d,
+                            c.scale, causal, dcode, sh), "fa_bwd")
+    elif w["kind"] == "decode":
         ws_bytes = int(lib.fa_decode_workspace_size(B, H, Hkv, Nq, Nk, d))
         ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
         launches = 2 if ws_bytes > 0 else 1
@@ -400,6 +439,19 @@ def run_extra(args, w, local_rank):
     if status != 0:
         raise RuntimeError(f"a kernel reported {fa.STATUS.get(status)} in the timed region")
     t = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)   # ms per step
+    t_dense = None
+    if dense_step is not None:   # the same step with the dense kernels, for the speed-up
+        for _ in range(args.warmup):
+            flush.zero_()
+            dense_step()
+        ts = []
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(stream)
+            dense_step()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        t_dense = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
     cfg = {"workload": f"{args.workload}: B={B} H={H} Hkv={Hkv} Nq={Nq} Nk={Nk} d={d} {w['dtype']} "
                        f"{'causal (bottom-right)' if causal else 'non-causal'}"
                        f"{' fwd+bwd' if w['backward'] else ''}",
@@ -408,7 +460,21 @@ def run_extra(args, w, local_rank):
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w["dtype"],
            "data": "synthetic (seeded i.i.d. N(0,1) 16-bit inputs)", "config": cfg,
            "gpu_launches": launches * args.steps}
-    if w["kind"] == "decode":
+    if w["kind"] == "sparse":
+        pairs = H * B * butterfly_visible_pairs(Nq, bool(causal))
+        f = pairs * d * 14
+        tf = f / (t * 1e-3) / 1e12
+        peak_burst, peak_sus, src = measured_peaks()
+        res.update({"metric": "block-sparse attention TFLOPS over the pattern's (query, key) pairs "
+                              "(fa_fwd_sparse + fa_bwd_sparse)",
+                    "value": round(tf, 2), "unit": UNIT,
+                    "speedup_vs_dense": round(t_dense / t, 3), "dense_ms_per_step": round(t_dense, 5),
+                    "pattern_density": round(pairs / (H * B * (Nq * Nq if not causal else Nq * (Nq + 1) / 2)), 5),
+                    "roofline": {"bound": "tensor", "kernel": "fwd_kernel + bwd_kv_kernel", "achieved": round(tf, 2),
+                                 "peak": peak_sus, "unit": UNIT, "frac": round(tf / peak_sus, 4),
+                                 "frac_of_burst_peak": round(tf / peak_burst, 4),
+                                 "peak_source": f"{src} bf16 cuBLAS sustained", "traffic": None}})
+    elif w["kind"] == "decode":
         nbytes = 2 * B * Hkv * Nk * d * 2 + 2 * B * H * Nq * d * 2 + B * H * Nq * 4
         gbs = nbytes / (t * 1e-3) / 1e9
         hbm, src = 6800.0, "fallback"

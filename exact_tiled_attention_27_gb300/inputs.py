@@ -155,6 +155,9 @@ EXTRA_WORKLOADS = {
                           backward=False, index=22),
     "x4_decode_mha": dict(kind="decode", B=16, H=32, Hkv=32, Nq=1, Nk=8192, d=128, dtype="bf16", causal=True,
                           backward=False, index=23),
+    # block-sparse (butterfly) training step at long sequence length
+    "x5_butterfly_64k": dict(kind="sparse", B=1, H=16, Hkv=16, Nq=65536, Nk=65536, d=64, dtype="bf16",
+                             causal=False, backward=True, index=24),
 }
 
 

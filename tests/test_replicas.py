@@ -63,3 +63,16 @@ def test_cross_visible_pairs_closed_forms():
     assert bench.cross_visible_pairs(10, 4, True) == sum(range(1, 5))          # six rows see nothing
     nq, nk = 300, 1000
     assert bench.cross_visible_pairs(nq, nk, True) == nq * (nk - nq) + nq * (nq + 1) // 2
+
+
+def test_butterfly_visible_pairs_counts():
+    """FLOP count of the block-sparse workload against the oracle's own mask."""
+    import bench
+    import numpy as np
+    from oracle import attention as A
+    for n, causal in ((256, False), (1000, False), (1000, True), (1300, True), (2048, False)):
+        want = int(A.butterfly_mask(n, n, causal).sum())
+        assert bench.butterfly_visible_pairs(n, causal) == want, (n, causal)
+    assert bench.butterfly_visible_pairs(256, True) == 256 * 257 // 2
+    # 2^15 keys = 128 blocks of 256: each links 1 + log2(128) = 8 of them
+    assert np.isclose(bench.butterfly_visible_pairs(1 << 15, False) / (1 << 30), 8 / 128)
