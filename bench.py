@@ -484,7 +484,7 @@ def run_extra(args, w, local_rank):
                 hbm, src = float(json.load(f)["hbm_gbs"]), "measured"
         res.update({"metric": "decode: bytes of K, V, Q, O and lse moved per second", "value": round(gbs, 1),
                     "unit": "GB/s",
-                    "roofline": {"bound": "hbm", "kernel": "decode_split_kernel", "achieved": round(gbs, 1),
+                    "roofline": {"bound": "hbm", "kernel": "decode_split_kernel_d64|d128", "achieved": round(gbs, 1),
                                  "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
                                  "peak_source": f"{src} copy bandwidth", "traffic": None}})
     else:

@@ -8,7 +8,7 @@
 // few heads, the keys of a head are cut into S contiguous ranges ("splits"), one CTA
 // per (split, key/value head):
 //
-//   decode_split_kernel   for its key range: the scores, the streaming (m, l)
+//   decode_split_kernel_* for its key range: the scores, the streaming (m, l)
 //                         softmax and the unnormalised sum of P V for each query row,
 //                         then O_s = sum / l and lse_s = m + ln l of that range.
 //   decode_merge_kernel   (S > 1) combines the ranges: lse = ln sum_s e^{lse_s},
@@ -22,7 +22,7 @@
 // in the forward kernel.  The causal mask is aligned bottom-right (query i of Nq sees
 // key j iff j <= i + Nk - Nq), so a single new token sees the whole cache.
 //
-// Work split inside decode_split_kernel: a warp takes 32 consecutive keys at a time.
+// Work split inside decode_split: a warp takes 32 consecutive keys at a time.
 // For the scores each lane owns one key (its row of K is read 16 bytes at a time, the
 // query rows are broadcast from shared memory), so a score needs no cross-lane sum;
 // the running maximum moves once per 32 keys (one warp reduction per query row).  For
@@ -30,6 +30,8 @@
 // V rows (coalesced) and the 32 probabilities from shared memory.  Each warp keeps
 // its own (m, l, O) over the keys it visited; the CTA merges its warps at the end.
 #include <cuda_fp16.h>
+
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -50,12 +52,16 @@ __device__ __forceinline__ size_t query_row(int bhk, int m, int H, int Hkv, int 
   return (size_t)(b * H + hk * G + g) * Nq + qi;
 }
 
+// d = 64: each lane's V columns of the step are requested up front with its K row (32
+// more registers; one CTA per SM keeps enough bytes in flight).  d = 128: that would cost
+// 64 registers and the CTAs per SM that hide the latency, so V is read in the P V loop.
 template <int D, int DT, int MR>
-__global__ void __launch_bounds__(kDecThreads) decode_split_kernel(
+__device__ __forceinline__ void decode_split(
     const uint16_t* __restrict__ q, const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
     float* __restrict__ opart, float* __restrict__ lpart, uint16_t* __restrict__ out, float* __restrict__ lse,
     int H, int Hkv, int Nq, int Nk, int M, int chunk, float scale_log2, int causal) {
   constexpr int kCols = D / 32;                // output columns per lane
+  constexpr bool kVEarly = (D == 64);
   __shared__ __align__(16) float sq[MR][D];    // query rows times scale*log2(e)
   __shared__ __align__(16) float sp[kDecWarps][32][MR];
   __shared__ float sm_m[kDecWarps][MR];
@@ -105,11 +111,24 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(
   for (int j0 = k0 + warp * 32; j0 < k1; j0 += 32 * kDecWarps) {   // uniform in the warp
     const int j = j0 + lane;
     const bool live = j < k1;
-    // ---- scores of key j for every query row
+    // ---- this lane's K row and its columns of the 32 V rows, all requested up front so
+    // that the whole step's bytes are in flight while the scores are formed
     uint4 kr[D / 8];
 #pragma unroll
     for (int c8 = 0; c8 < D / 8; ++c8)
       kr[c8] = live ? __ldg(reinterpret_cast<const uint4*>(kh + (size_t)j * D + c8 * 8)) : make_uint4(0u, 0u, 0u, 0u);
+    using VW = typename std::conditional<kCols == 2, unsigned int, uint2>::type;
+    auto load_v = [&](int kk) -> VW {
+      if (j0 + kk < k1) return __ldg(reinterpret_cast<const VW*>(vh + (size_t)(j0 + kk) * D + lane * kCols));
+      if constexpr (kCols == 2) return 0u;
+      else return make_uint2(0u, 0u);
+    };
+    VW vr[kVEarly ? 32 : 1];
+    (void)vr;
+    if constexpr (kVEarly) {
+#pragma unroll
+      for (int kk = 0; kk < 32; ++kk) vr[kk] = load_v(kk);
+    }
     float dot[MR];
 #pragma unroll
     for (int m = 0; m < MR; ++m) dot[m] = 0.f;
@@ -165,19 +184,16 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(
       for (int m = 0; m < MR; ++m) pw[lane * MR + m] = p[m];
     }
     __syncwarp();
-    // ---- O += P V: this lane's columns of the 32 V rows
-    const int nk = min(32, k1 - j0);
-#pragma unroll 8
-    for (int kk = 0; kk < nk; ++kk) {
-      const uint16_t* vrow = vh + (size_t)(j0 + kk) * D + lane * kCols;
+    // ---- O += P V: this lane's columns of the 32 V rows (rows past the range hold
+    // zeros and have P = 0)
+    auto pv_row = [&](int kk, VW vw) {
       float vf[kCols];
       if constexpr (kCols == 2) {
-        const float2 f = unpack2<DT>(__ldg(reinterpret_cast<const unsigned int*>(vrow)));
+        const float2 f = unpack2<DT>(vw);
         vf[0] = f.x;
         vf[1] = f.y;
       } else {
-        const uint2 w = __ldg(reinterpret_cast<const uint2*>(vrow));
-        const float2 f0 = unpack2<DT>(w.x), f1 = unpack2<DT>(w.y);
+        const float2 f0 = unpack2<DT>(vw.x), f1 = unpack2<DT>(vw.y);
         vf[0] = f0.x;
         vf[1] = f0.y;
         vf[2] = f1.x;
@@ -202,6 +218,14 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(
 #pragma unroll
         for (int c = 0; c < kCols; ++c) acc[m][c] = fmaf(pk[m], vf[c], acc[m][c]);
       }
+    };
+    if constexpr (kVEarly) {
+#pragma unroll
+      for (int kk = 0; kk < 32; ++kk) pv_row(kk, vr[kk]);
+    } else {
+      const int nk = min(32, k1 - j0);
+#pragma unroll 8
+      for (int kk = 0; kk < nk; ++kk) pv_row(kk, load_v(kk));
     }
     __syncwarp();
   }
@@ -255,6 +279,22 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(
   grid_dep_launch();
 }
 
+template <int DT, int MR>
+__global__ void __launch_bounds__(kDecThreads, 1) decode_split_kernel_d64(
+    const uint16_t* __restrict__ q, const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
+    float* __restrict__ opart, float* __restrict__ lpart, uint16_t* __restrict__ out, float* __restrict__ lse,
+    int H, int Hkv, int Nq, int Nk, int M, int chunk, float scale_log2, int causal) {
+  decode_split<64, DT, MR>(q, k, v, opart, lpart, out, lse, H, Hkv, Nq, Nk, M, chunk, scale_log2, causal);
+}
+
+template <int DT, int MR>
+__global__ void __launch_bounds__(kDecThreads) decode_split_kernel_d128(
+    const uint16_t* __restrict__ q, const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
+    float* __restrict__ opart, float* __restrict__ lpart, uint16_t* __restrict__ out, float* __restrict__ lse,
+    int H, int Hkv, int Nq, int Nk, int M, int chunk, float scale_log2, int causal) {
+  decode_split<128, DT, MR>(q, k, v, opart, lpart, out, lse, H, Hkv, Nq, Nk, M, chunk, scale_log2, causal);
+}
+
 // One thread per (key/value head, query row, 8-column segment): combine the S ranges.
 template <int D, int DT>
 __global__ void __launch_bounds__(256) decode_merge_kernel(const float* __restrict__ opart,
@@ -302,7 +342,8 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const float* __restri
 
 template <int D, int DT, int MR>
 cudaError_t launch_decode_t(const DecArgs& a, cudaStream_t stream) {
-  cudaError_t e = launch_overlapped(decode_split_kernel<D, DT, MR>, dim3(a.S, a.BHkv), kDecThreads, 0, stream,
+  auto kern = D == 64 ? decode_split_kernel_d64<DT, MR> : decode_split_kernel_d128<DT, MR>;
+  cudaError_t e = launch_overlapped(kern, dim3(a.S, a.BHkv), kDecThreads, 0, stream,
                                     static_cast<const uint16_t*>(a.q), static_cast<const uint16_t*>(a.k),
                                     static_cast<const uint16_t*>(a.v), a.opart, a.lpart,
                                     static_cast<uint16_t*>(a.o), a.lse, a.H, a.Hkv, a.Nq, a.Nk, a.M, a.chunk,
