@@ -486,7 +486,8 @@ def run_extra(args, w, local_rank):
                     "unit": "GB/s",
                     "roofline": {"bound": "hbm", "kernel": "decode_split_kernel_d64|d128", "achieved": round(gbs, 1),
                                  "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
-                                 "peak_source": f"{src} copy bandwidth", "traffic": None}})
+                                 "peak_source": f"{src} copy bandwidth",
+                                 "traffic": traffic_for("decode_split_kernel", args.workload)}})
     else:
         pairs = H * B * cross_visible_pairs(Nq, Nk, bool(causal))
         f = pairs * d * (4 + (10 if w["backward"] else 0))
@@ -504,7 +505,7 @@ def run_extra(args, w, local_rank):
     return res
 
 
-KERNEL_SOURCE = {"fwd_kernel": "fwd.cu", "bwd_kv_kernel": "bwd.cu"}
+KERNEL_SOURCE = {"fwd_kernel": "fwd.cu", "bwd_kv_kernel": "bwd.cu", "decode_split_kernel": "decode.cu"}
 
 
 def source_sha256(kernel):
