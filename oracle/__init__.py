@@ -25,8 +25,12 @@ materialising the score matrix S and the probability matrix P on purpose:
 * ``butterfly_mask`` / ``attn_masked_head_fwd`` / ``attn_masked_head_bwd`` -- the
   definition with a boolean visibility mask, and the fixed butterfly block pattern of
   block-sparse attention.
+* ``fp8`` -- the E4M3 format (``e4m3_encode`` / ``e4m3_decode``), the fixed random
+  rotation of Q and K (``rotate_exact``, ``rotate_fp32``), block quantization
+  (``quantize_blocks`` / ``dequantize_blocks``) and the FP8 forward's reference
+  (``attn_fp8_ref``: exact attention on the de-quantised inputs).
 
-Parity pins: every function here is pinned by tests in ``tests/test_oracle_pins.py``
+Parity pins: every function here is pinned by tests in ``tests/test_oracle_*pins.py``
 against printed worked examples, closed forms, invariants, library routines and
 central finite differences.  No function is "parity unpinned".
 """
@@ -50,4 +54,17 @@ from .attention import (  # noqa: F401
     butterfly_mask,
     attn_masked_head_fwd,
     attn_masked_head_bwd,
+)
+from .fp8 import (  # noqa: F401
+    E4M3_MAX,
+    QUANT_BLOCK,
+    e4m3_values,
+    e4m3_decode,
+    e4m3_encode,
+    hadamard,
+    rotate_exact,
+    rotate_fp32,
+    quantize_blocks,
+    dequantize_blocks,
+    attn_fp8_ref,
 )
