@@ -23,6 +23,9 @@ from .binding import (  # noqa: F401
     device_sm_count,
     forward,
     forward_cross,
+    forward_fp8,
+    fp8_vt_cols,
+    quantize_fp8,
     last_kernel_status,
     load_library,
     strerror,

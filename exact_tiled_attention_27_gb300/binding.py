@@ -75,6 +75,12 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.fa_bwd_noalloc.restype = i
         lib.fa_bwd_noalloc_max_scratch.argtypes = []
         lib.fa_bwd_noalloc_max_scratch.restype = sz
+        lib.fa_fp8_vt_cols.argtypes = [i]
+        lib.fa_fp8_vt_cols.restype = i
+        lib.fa_quantize_fp8.argtypes = [vp, vp, vp, i, i, i, i, i, vp, i, i, vp]
+        lib.fa_quantize_fp8.restype = i
+        lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
+        lib.fa_fwd_fp8.restype = i
         lib.fa_strerror.argtypes = [i]
         lib.fa_strerror.restype = ctypes.c_char_p
         lib.fa_get_last_kernel_status.argtypes = [vp]
@@ -306,3 +312,65 @@ def device_sm_count() -> int:
 
 def debug_wait_timeout(limit_us: int, stream=None) -> int:
     return int(load_library().fa_debug_wait_timeout(int(limit_us), _stream_handle(stream)))
+
+
+# ----------------------------------------------------------------------------- FP8 forward
+def fp8_vt_cols(N) -> int:
+    """Row length Nt (bytes) of the transposed V codes: N rounded up to 16."""
+    return (int(N) + 15) // 16 * 16
+
+
+def quantize_fp8(x, per_tensor=False, signs=None, transpose=False, stream=None):
+    """E4M3 codes and per-128-row-block float32 scales of x (B, H, N, d) bf16/fp16
+    (fa_quantize_fp8).  ``signs``: optional (d,) float32 CUDA tensor of +-1 -- rows are
+    then rotated by diag(signs) H / sqrt(d) first (use the same signs for q and k).
+    ``transpose=True`` gives the (B, H, d, Nt) V^T layout ``forward_fp8`` reads.
+
+    Returns (codes uint8, scales float32 (B, H, ceil(N/128)))."""
+    torch = _torch()
+    B, H, N, d = x.shape
+    _check_bhnd("x", x, (B, H, N, d), x.dtype)
+    nb = (N + 127) // 128
+    codes = torch.empty((B, H, d, fp8_vt_cols(N)) if transpose else (B, H, N, d), dtype=torch.uint8,
+                        device=x.device)
+    scales = torch.empty((B, H, nb), dtype=torch.float32, device=x.device)
+    sp = None
+    if signs is not None:
+        if not signs.is_cuda or signs.dtype != torch.float32 or tuple(signs.shape) != (d,) or not signs.is_contiguous():
+            raise ValueError("signs must be a contiguous float32 CUDA tensor of shape (d,)")
+        sp = _ptr(signs)
+    st = load_library().fa_quantize_fp8(_ptr(x), _ptr(codes), _ptr(scales), B, H, N, d, _dtype_code(x), sp,
+                                        1 if per_tensor else 0, 1 if transpose else 0, _stream_handle(stream))
+    if st != 0:
+        raise FaError(st, "fa_quantize_fp8")
+    return codes, scales
+
+
+def forward_fp8(q8, k8, vt8, q_scale, k_scale, v_scale, scale=None, causal=False, out_dtype=None, out=None,
+                lse=None, stream=None):
+    """FP8 forward (fa_fwd_fp8): q8, k8 (B, H, N, d) and vt8 (B, H, d, Nt) uint8 E4M3 codes
+    with (B, H, ceil(N/128)) float32 block scales, as made by ``quantize_fp8``.  ``scale``
+    defaults to d ** -0.5.  Returns (o, lse): o (B, H, N, d) in ``out_dtype`` (bfloat16 by
+    default), lse float32 (B, H, N)."""
+    torch = _torch()
+    B, H, N, d = q8.shape
+    nb = (N + 127) // 128
+    out_dtype = torch.bfloat16 if out_dtype is None else out_dtype
+    _check_bhnd("q8", q8, (B, H, N, d), torch.uint8)
+    _check_bhnd("k8", k8, (B, H, N, d), torch.uint8)
+    _check_bhnd("vt8", vt8, (B, H, d, fp8_vt_cols(N)), torch.uint8)
+    for name, t in (("q_scale", q_scale), ("k_scale", k_scale), ("v_scale", v_scale)):
+        _check_bhnd(name, t, (B, H, nb), torch.float32)
+    scale = float(d) ** -0.5 if scale is None else float(scale)
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=out_dtype, device=q8.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
+    _check_bhnd("out", out, (B, H, N, d), out_dtype)
+    _check_bhnd("lse", lse, (B, H, N), torch.float32)
+    st = load_library().fa_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(vt8), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale),
+                                   _ptr(out), _ptr(lse), B, H, N, d, scale, 1 if causal else 0, _dtype_code(out),
+                                   _stream_handle(stream))
+    if st != 0:
+        raise FaError(st, "fa_fwd_fp8")
+    return out, lse

@@ -24,8 +24,8 @@ BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libfa_gb300.so")
 
-SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "decode.cu", "noalloc.cu"]
-HEADERS = ["ptx.cuh", "internal.h"]
+SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "decode.cu", "noalloc.cu", "fwd_fp8.cu", "quant.cu"]
+HEADERS = ["ptx.cuh", "internal.h", "fwd_tiles.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
          f"-I{INCLUDE}", f"-I{CSRC}"]

@@ -100,6 +100,35 @@ bool encode_accum(CUtensorMap* m, void* base, int BH, int N, int d) {
   return r == CUDA_SUCCESS;
 }
 
+// 3-D map over contiguous (B*H, N, d) E4M3 codes: box of 128 rows x d bytes, 64-byte
+// swizzle at d = 64 and 128-byte at d = 128 (one swizzle row per tensor row).
+bool encode_fp8_rows(CUtensorMap* m, const void* base, int BH, int N, int d) {
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  const cuuint64_t strides[2] = {(cuuint64_t)d, (cuuint64_t)N * d};
+  const cuuint32_t box[3] = {(cuuint32_t)d, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              d == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 3-D map over V^T codes (B*H, d, Nt): box of d rows x 128 keys, 128-byte swizzle; keys
+// past N read as zero whatever the padding holds.
+bool encode_fp8_vt(CUtensorMap* m, const void* base, int BH, int N, int Nt, int d) {
+  const cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)d, (cuuint64_t)BH};
+  const cuuint64_t strides[2] = {(cuuint64_t)Nt, (cuuint64_t)Nt * d};
+  const cuuint32_t box[3] = {128, (cuuint32_t)d, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int fp8_vt_cols(int N) { return (N + 15) / 16 * 16; }
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int check_common(int B, int H, int N, int d, float scale, int dtype) {
@@ -210,6 +239,69 @@ int fa_fwd_sparse(const void* q, const void* k, const void* v, void* o, float* l
                   float scale, int causal, int pattern, int dtype, void* stream) {
   if (pattern != FA_PATTERN_BUTTERFLY) return FA_ERR_PATTERN;
   return fwd_common(q, k, v, o, lse, B, H, H, N, N, d, scale, causal, dtype, stream, 1);
+}
+
+int fa_fp8_vt_cols(int N) { return N >= 1 ? fp8_vt_cols(N) : 0; }
+
+int fa_quantize_fp8(const void* x, void* x8, float* scales, int B, int H, int N, int d, int dtype, const float* signs,
+                    int per_tensor, int transpose, void* stream) {
+  int st = check_common(B, H, N, d, 1.0f, dtype);
+  if (st != FA_OK) return st;
+  if (!x || !x8 || !scales) return FA_ERR_NULL;
+  if (!aligned16(x) || !aligned16(x8) || (reinterpret_cast<uintptr_t>(scales) & 3u) ||
+      (reinterpret_cast<uintptr_t>(signs) & 3u))
+    return FA_ERR_ALIGN;
+  DeviceInfo* dev = nullptr;
+  st = get_device(&dev);
+  if (st != FA_OK) return st;
+  QuantArgs a;
+  a.x = x;
+  a.x8 = x8;
+  a.scales = scales;
+  a.signs = signs;
+  a.BH = B * H;
+  a.N = N;
+  a.d = d;
+  a.dtype = dtype;
+  a.per_tensor = per_tensor ? 1 : 0;
+  a.transpose = transpose ? 1 : 0;
+  a.Nt = fp8_vt_cols(N);
+  return launch_quantize_fp8(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+int fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_scale, const float* k_scale,
+               const float* v_scale, void* o, float* lse, int B, int H, int N, int d, float scale, int causal,
+               int dtype, void* stream) {
+  int st = check_common(B, H, N, d, scale, dtype);
+  if (st != FA_OK) return st;
+  if (!q8 || !k8 || !vt8 || !q_scale || !k_scale || !v_scale || !o || !lse) return FA_ERR_NULL;
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(vt8) || !aligned16(o) ||
+      ((reinterpret_cast<uintptr_t>(q_scale) | reinterpret_cast<uintptr_t>(k_scale) |
+        reinterpret_cast<uintptr_t>(v_scale) | reinterpret_cast<uintptr_t>(lse)) & 3u))
+    return FA_ERR_ALIGN;
+  DeviceInfo* dev = nullptr;
+  st = get_device(&dev);
+  if (st != FA_OK) return st;
+  FwdF8Args a;
+  const int BH = B * H;
+  if (!encode_fp8_rows(&a.tm_q, q8, BH, N, d) || !encode_fp8_rows(&a.tm_k, k8, BH, N, d) ||
+      !encode_fp8_vt(&a.tm_vt, vt8, BH, N, fp8_vt_cols(N), d))
+    return FA_ERR_LAUNCH;
+  a.q_scale = q_scale;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.o = o;
+  a.lse = lse;
+  a.BH = BH;
+  a.N = N;
+  a.d = d;
+  a.dtype = dtype;
+  a.causal = causal ? 1 : 0;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.err_word = dev->err_word;
+  a.limit_ns = kWaitLimitNs;
+  a.num_sms = dev->num_sms;
+  return launch_fwd_fp8(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 int fa_butterfly_blocks(int nblocks, int pair, int causal_dir, int* out, int cap) {

@@ -174,4 +174,32 @@ constexpr int kBwdStageDQ = 4;
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream, int stages);
 cudaError_t launch_debug_wait(unsigned int* err_word, uint64_t limit_ns, cudaStream_t stream);
 
+// FP8 (E4M3) forward, Nq = Nk, one key/value head per query head.
+struct FwdF8Args {
+  CUtensorMap tm_q, tm_k;   // 3-D maps {d, N, B*H} of 8-bit codes, box {d, 128, 1},
+                            // 64-byte (d = 64) or 128-byte (d = 128) swizzle
+  CUtensorMap tm_vt;        // 3-D map {N, d, B*H} over V^T (row stride Nt bytes), box {128, d, 1}
+  const float* q_scale;     // [B*H, nb] per 128-row block
+  const float* k_scale;
+  const float* v_scale;
+  void* o;                  // [B, H, N, d] 16-bit
+  float* lse;
+  int BH, N, d, dtype, causal;
+  float scale_log2;
+  unsigned int* err_word;
+  uint64_t limit_ns;
+  int num_sms;
+};
+cudaError_t launch_fwd_fp8(const FwdF8Args& a, cudaStream_t stream);
+
+// E4M3 block quantization: per-block amax, scales, codes (three launches).
+struct QuantArgs {
+  const void* x;            // [B*H, N, d] 16-bit
+  void* x8;                 // [B*H, N, d] codes, or [B*H, d, Nt] when transpose
+  float* scales;            // [B*H, nb]
+  const float* signs;       // [d] +-1, or nullptr for no rotation
+  int BH, N, d, dtype, per_tensor, transpose, Nt;
+};
+cudaError_t launch_quantize_fp8(const QuantArgs& a, cudaStream_t stream);
+
 }  // namespace fa

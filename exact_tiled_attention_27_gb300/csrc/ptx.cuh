@@ -208,6 +208,18 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       : "memory");
 }
 
+// D(tmem) (+)= A(smem desc) * B(smem desc), kind::f8f6f4 (8-bit in, fp32 accumulate;
+// 32 elements of K per instruction).
+__device__ __forceinline__ void umma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "setp.ne.b32 P, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, P;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05.mma issued so far by this thread has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -225,6 +237,19 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t start, uint32_t lbo, ui
   return static_cast<uint64_t>((start & 0x3FFFFu) >> 4) |
          (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
          (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Shared-memory matrix descriptor, 64-byte swizzle (layout type 4): K-major operands
+// whose rows are 64 bytes (64 8-bit elements); 8-row groups are 512 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t start, uint32_t sbo) {
+  return static_cast<uint64_t>((start & 0x3FFFFu) >> 4) | (1ull << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (4ull << 61);
+}
+
+// Instruction descriptor for kind::f8f6f4 with E4M3 A and B (format code 0), both
+// K-major, fp32 accumulation.
+__host__ __device__ constexpr uint32_t idesc_e4m3(uint32_t M, uint32_t N) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
 // Instruction descriptor for kind::f16 with fp32 accumulation.
@@ -322,6 +347,15 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
   }
   return d;
+}
+
+// four floats -> four E4M3 codes (round to nearest even, saturating at +-448) in one
+// word, a -> bits 0..7, b -> 8..15, c -> 16..23, d -> 24..31
+__device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float d) {
+  uint16_t lo, hi;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
 template <int DT>

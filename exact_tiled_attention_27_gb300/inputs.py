@@ -172,3 +172,26 @@ def workload_case(name: str, with_do=None) -> Case:
     wd = w["backward"] if with_do is None else with_do
     return make_case(w["B"], w["H"], w["N"], w["d"], w["dtype"], w["causal"], None,
                      w["index"], w.get("length_index", 0), w["mult"], wd)
+
+
+def random_signs(d: int, seed: int) -> np.ndarray:
+    """d random signs (+1.0 / -1.0, float32) from PCG64(seed): the random draw of the
+    fixed rotation that multiplies Q and K before FP8 rounding.  Drawn here and passed
+    to both sides as an input."""
+    rng = np.random.Generator(np.random.PCG64(int(seed)))
+    return np.where(rng.random(int(d)) < 0.5, -1.0, 1.0).astype(np.float32)
+
+
+def with_outlier_channel(bits: np.ndarray, dtype: str, channel: int, factor: float) -> np.ndarray:
+    """The same 16-bit values with column `channel` multiplied by `factor` (rounded back
+    to `dtype`): the outlier channel of the FP8 error study."""
+    x = bits_to_f64(bits, dtype)
+    x[..., channel] *= factor
+    return f64_to_bits(x, dtype)
+
+
+def with_outlier_entry(bits: np.ndarray, dtype: str, index: tuple, value: float) -> np.ndarray:
+    """The same 16-bit values with one entry set to `value`: an isolated outlier."""
+    x = bits_to_f64(bits, dtype)
+    x[index] = value
+    return f64_to_bits(x, dtype)

@@ -210,6 +210,42 @@ int fa_bwd_sparse(const void* q, const void* k, const void* v, const void* o, co
 int fa_butterfly_blocks(int nblocks, int pair, int causal_dir, int* out, int cap);
 
 /*
+ * FP8 forward ("Flash Attention" chapter, mlx.void.app, section "FlashAttention-3——重叠
+ * 与低精度": E4M3 numbers, block quantization, and a fixed random rotation of Q and K
+ * applied before rounding).
+ *
+ * fa_quantize_fp8: E4M3 codes and per-block scales of a 16-bit (B, H, N, d) tensor.
+ *   x          : in,  (B, H, N, d) `dtype`, 16-byte aligned
+ *   x8         : out, E4M3 codes, 16-byte aligned: (B, H, N, d) bytes, or with
+ *                `transpose` (B, H, d, Nt) bytes with Nt = fa_fp8_vt_cols(N) -- the V^T
+ *                layout fa_fwd_fp8 reads (keys N .. Nt-1 are written as +0)
+ *   scales     : out, (B, H, ceil(N/128)) float32: block j of a head holds rows
+ *                128j .. 128j+127 and represents code * scales[j]
+ *   signs      : NULL, or d floats of +-1 (device memory): rows are first multiplied by
+ *                the rotation diag(signs) H / sqrt(d) (H the Sylvester-Hadamard matrix);
+ *                give the same signs for Q and K, none for V
+ *   per_tensor : 0: scale = amax(block) / 448 per block; 1: the head's amax for every
+ *                block (one scale per (b, h) -- the failure mode block scales avoid)
+ *   Blocks whose values are all 0 get scale 1.  Codes round to nearest even and
+ *   saturate at +-448.  Three launches on `stream`; errors as fa_fwd.
+ *
+ * fa_fwd_fp8: O and lse from E4M3 codes, Nq = Nk = N, one key/value head per query head.
+ *   q8, k8     : in, (B, H, N, d) E4M3 codes; vt8 : in, (B, H, d, Nt) codes of V^T
+ *   q_scale, k_scale, v_scale : in, (B, H, ceil(N/128)) float32 block scales (> 0)
+ *   o, lse     : out as fa_fwd, o in `dtype` (bf16 or fp16)
+ *   The products run on the 8-bit tensor-core path with fp32 accumulation; P is rounded
+ *   to E4M3 (relative error up to 2^-4 per entry) before P.V, so O carries that error on
+ *   top of the inputs' quantization; lse uses the unrounded P.
+ * Both return FA_OK or an fa_status error code, validated before any launch.
+ */
+int fa_fp8_vt_cols(int N);
+int fa_quantize_fp8(const void* x, void* x8, float* scales, int B, int H, int N, int d, int dtype,
+                    const float* signs, int per_tensor, int transpose, void* stream);
+int fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_scale,
+               const float* k_scale, const float* v_scale, void* o, float* lse, int B, int H,
+               int N, int d, float scale, int causal, int dtype, void* stream);
+
+/*
  * The three stages fa_bwd runs, one launch each, for callers that want to time or
  * schedule them separately.  Arguments, validation and errors are exactly fa_bwd's;
  * calling the three in this order on one stream with one workspace is fa_bwd.

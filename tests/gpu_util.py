@@ -10,6 +10,15 @@ Tolerances (stated for the 16-bit inputs against the float64 oracle):
                 up to 0.031 > 2e-2.
   lse:          max |err| <= 1e-3
   dQ, dK, dV:   ||err||_2 / ||ref||_2 <= 1e-2
+
+FP8 forward (against exact attention on the de-quantised inputs, so that only what the
+kernel adds is measured): P is rounded to E4M3 before P.V.  Round-to-nearest with a
+3-bit mantissa errs by at most 2^-4 of a value and, over a binade, by 2^-4/sqrt(3)
+root-mean-square at most; with independent errors over many keys O's relative L2
+error is at most that RMS (0.036), and in the worst case, every error aligned, one
+row of O is off by 2^-4 max|V|.  Hence:
+  O:            max |err| <= 2^-4 * max|V| + 1e-2  and  relL2 <= 4e-2
+  lse:          max |err| <= 1e-3 (it uses the unrounded P)
 """
 
 import numpy as np
@@ -18,6 +27,9 @@ O_MAXABS = 2e-2
 O_RELL2 = 5e-3
 LSE_ABS = 1e-3
 GRAD_RELL2 = 1e-2
+FP8_O_RELL2 = 4e-2
+FP8_O_MAXABS_PER_V = 2.0 ** -4
+FP8_O_MAXABS_EXTRA = 1e-2
 
 
 def torch_dtype(dtype):
@@ -62,3 +74,13 @@ def check_backward(grads, refs, label=""):
         assert np.all(np.isfinite(g)), msg
     assert max(errs) <= GRAD_RELL2, msg
     return errs
+
+
+def check_forward_fp8(o, lse, o_ref, lse_ref, vmax, label=""):
+    ma, rl, la = maxabs(o, o_ref), rel_l2(o, o_ref), maxabs(lse, lse_ref)
+    bound = FP8_O_MAXABS_PER_V * vmax + FP8_O_MAXABS_EXTRA
+    msg = f"{label} O maxabs={ma:.3e} (bound {bound:.2e}) relL2={rl:.3e} lse abs={la:.3e}"
+    print(msg)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse)), msg
+    assert ma <= bound and rl <= FP8_O_RELL2 and la <= LSE_ABS, msg
+    return ma, rl, la

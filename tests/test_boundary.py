@@ -115,6 +115,34 @@ def test_backward_gqa_validation_codes(lib):
     assert call(ws_bytes=need - 1) == C["FA_ERR_WORKSPACE"]
 
 
+def test_fp8_entry_points_validate(lib):
+    C = binding.STATUS_CODE
+    assert [lib.fa_fp8_vt_cols(n) for n in (0, 1, 16, 17, 1000)] == [0, 16, 16, 32, 1008]
+
+    def quant(x=P, x8=P, scales=P, B=1, H=1, N=128, d=64, dtype=0, signs=NULL):
+        return lib.fa_quantize_fp8(x, x8, scales, B, H, N, d, dtype, signs, 0, 0, NULL)
+
+    assert quant(x=NULL) == C["FA_ERR_NULL"]
+    assert quant(scales=NULL) == C["FA_ERR_NULL"]
+    assert quant(d=80) == C["FA_ERR_UNSUPPORTED_D"]
+    assert quant(dtype=3) == C["FA_ERR_DTYPE"]
+    assert quant(N=0) == C["FA_ERR_SHAPE"]
+    assert quant(x8=PM) == C["FA_ERR_ALIGN"]
+    assert quant(signs=ctypes.c_void_p(0x10002)) == C["FA_ERR_ALIGN"]
+
+    def f8(q=P, vt=P, ks=P, o=P, B=1, H=1, N=128, d=64, scale=0.125, dtype=0):
+        return lib.fa_fwd_fp8(q, P, vt, P, ks, P, o, P, B, H, N, d, scale, 1, dtype, NULL)
+
+    assert f8(q=NULL) == C["FA_ERR_NULL"]
+    assert f8(ks=NULL) == C["FA_ERR_NULL"]
+    assert f8(vt=PM) == C["FA_ERR_ALIGN"]
+    assert f8(ks=ctypes.c_void_p(0x10002)) == C["FA_ERR_ALIGN"]
+    assert f8(d=32) == C["FA_ERR_UNSUPPORTED_D"]
+    assert f8(dtype=2) == C["FA_ERR_DTYPE"]
+    assert f8(scale=0.0) == C["FA_ERR_SCALE"]
+    assert f8(B=0) == C["FA_ERR_SHAPE"]
+
+
 def test_decode_validation_and_workspace(lib):
     C = binding.STATUS_CODE
 
