@@ -397,6 +397,28 @@ def run_extra(args, w, local_rank):
             call(lib.fa_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, Nq, d, c.scale, causal, dcode, sh), "fa_fwd")
             call(lib.fa_bwd(P(q), P(k), P(v), P(o), P(do), P(lse), P(dq), P(dk), P(dv), P(ws), ws_bytes, B, H, Nq, d,
                             c.scale, causal, dcode, sh), "fa_bwd")
+    elif w["kind"] == "fp8":
+        from exact_tiled_attention_27_gb300.inputs import random_signs
+        signs = torch.from_numpy(random_signs(d, 1000 * w["index"] + 7)).to(dev)
+        nb = (Nq + 127) // 128
+        q8 = torch.empty((B, H, Nq, d), dtype=torch.uint8, device=dev)
+        k8 = torch.empty_like(q8)
+        vt8 = torch.empty((B, H, d, lib.fa_fp8_vt_cols(Nq)), dtype=torch.uint8, device=dev)
+        sq, sk, sv = (torch.empty((B, H, nb), dtype=torch.float32, device=dev) for _ in range(3))
+
+        def quantize():
+            call(lib.fa_quantize_fp8(P(q), P(q8), P(sq), B, H, Nq, d, dcode, P(signs), 0, 0, sh), "fa_quantize_fp8")
+            call(lib.fa_quantize_fp8(P(k), P(k8), P(sk), B, H, Nq, d, dcode, P(signs), 0, 0, sh), "fa_quantize_fp8")
+            call(lib.fa_quantize_fp8(P(v), P(vt8), P(sv), B, H, Nq, d, dcode, None, 0, 1, sh), "fa_quantize_fp8")
+
+        quantize()
+
+        def step():
+            call(lib.fa_fwd_fp8(P(q8), P(k8), P(vt8), P(sq), P(sk), P(sv), P(o), P(lse), B, H, Nq, d, c.scale,
+                                causal, dcode, sh), "fa_fwd_fp8")
+
+        def dense_step():   # the 16-bit forward on the same (unquantized) inputs
+            call(lib.fa_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, Nq, d, c.scale, causal, dcode, sh), "fa_fwd")
     elif w["kind"] == "decode":
         ws_bytes = int(lib.fa_decode_workspace_size(B, H, Hkv, Nq, Nk, d))
         ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
@@ -452,6 +474,18 @@ def run_extra(args, w, local_rank):
             e1.record(stream)
         torch.cuda.synchronize()
         t_dense = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
+    t_quant = None
+    if w["kind"] == "fp8":   # the three quantizing calls, timed the same way
+        for _ in range(args.warmup):
+            flush.zero_()
+            quantize()
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(stream)
+            quantize()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        t_quant = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
     cfg = {"workload": f"{args.workload}: B={B} H={H} Hkv={Hkv} Nq={Nq} Nk={Nk} d={d} {w['dtype']} "
                        f"{'causal (bottom-right)' if causal else 'non-causal'}"
                        f"{' fwd+bwd' if w['backward'] else ''}",
@@ -474,6 +508,27 @@ def run_extra(args, w, local_rank):
                                  "peak": peak_sus, "unit": UNIT, "frac": round(tf / peak_sus, 4),
                                  "frac_of_burst_peak": round(tf / peak_burst, 4),
                                  "peak_source": f"{src} bf16 cuBLAS sustained", "traffic": None}})
+    elif w["kind"] == "fp8":
+        pairs = H * B * cross_visible_pairs(Nq, Nk, bool(causal))
+        f = pairs * d * 4
+        tf = f / (t * 1e-3) / 1e12
+        peak_burst, peak_sus, src = measured_peaks()
+        # no measured FP8 peak: the measured bf16 one times the nominal dense ratio 4.5 / 2.25
+        p8_burst, p8_sus = 2 * peak_burst, 2 * peak_sus
+        res["dtype"] = "e4m3"
+        res["config"]["workload"] = (f"{args.workload}: B={B} H={H} N={Nq} d={d} E4M3 Q/K/V, 128-row block scales, "
+                                     f"Q and K rotated, {'causal' if causal else 'non-causal'} forward, "
+                                     f"{w['dtype']} O")
+        res.update({"metric": "FP8 attention forward TFLOPS (fa_fwd_fp8, 4*d flops per visible (query, key) pair)",
+                    "value": round(tf, 2), "unit": UNIT,
+                    "bf16_forward_ms": round(t_dense, 5), "speedup_vs_bf16_forward": round(t_dense / t, 3),
+                    "quantize_ms": round(t_quant, 5),
+                    "with_quantize_tflops": round(f / ((t + t_quant) * 1e-3) / 1e12, 2),
+                    "roofline": {"bound": "tensor", "kernel": "fwd_fp8_kernel", "achieved": round(tf, 2),
+                                 "peak": p8_sus, "unit": UNIT, "frac": round(tf / p8_sus, 4),
+                                 "frac_of_burst_peak": round(tf / p8_burst, 4),
+                                 "peak_source": f"{src} bf16 cuBLAS sustained x 2 (nominal fp8/bf16 dense ratio)",
+                                 "traffic": traffic_for("fwd_fp8_kernel", args.workload)}})
     elif w["kind"] == "decode":
         nbytes = 2 * B * Hkv * Nk * d * 2 + 2 * B * H * Nq * d * 2 + B * H * Nq * 4
         gbs = nbytes / (t * 1e-3) / 1e9
@@ -505,7 +560,8 @@ def run_extra(args, w, local_rank):
     return res
 
 
-KERNEL_SOURCE = {"fwd_kernel": "fwd.cu", "bwd_kv_kernel": "bwd.cu", "decode_split_kernel": "decode.cu"}
+KERNEL_SOURCE = {"fwd_kernel": "fwd.cu", "bwd_kv_kernel": "bwd.cu", "decode_split_kernel": "decode.cu",
+                 "fwd_fp8_kernel": "fwd_fp8.cu"}
 
 
 def source_sha256(kernel):

@@ -21,11 +21,14 @@
 //     y = s c_j + log2(sv_j), so P.V needs no per-block rescale of O, and the running
 //     sum l adds the same probabilities divided by sv_j.
 //   * P: rounded to E4M3 and written to shared memory (128 x 128 bytes, 128-byte
-//     swizzle, K-major A operand).  The running maximum M is exact (moved whenever a
-//     row maximum exceeds it) and P is formed as 2^(y - M + 8): the largest entry of a
-//     row is exactly 2^8 at the moment it sets the maximum, and entries down to
-//     2^-17 of it stay representable.  l is the sum of the unrounded values, and
-//     lse = (M - 8 + log2 l) ln 2.
+//     swizzle, K-major A operand).  The running maximum M only moves when a row
+//     maximum exceeds it by more than 4 (base 2), and P is formed as 2^(y - M + 4), so
+//     P <= 2^8 stays below E4M3's 448 and entries down to 2^-13 of a row's largest
+//     stay representable; O is rescaled only on the rare steps where M moves.
+//   * sums: l adds the unrounded P (lse = (M - 4 + log2 l) ln 2); lr, which divides O,
+//     adds them too but takes each block's largest P as rounded to E4M3.  A row
+//     dominated by one key is then normalised by the weight P.V actually used, and its
+//     O does not carry that weight's rounding error (up to 2^-4).
 #include <cuda_fp16.h>
 
 #include "fwd_tiles.cuh"
@@ -41,7 +44,8 @@ constexpr int kF8SoftmaxRegs = 216;
 constexpr int kF8OtherRegs = 64;
 static_assert((2 * kF8SoftmaxRegs + kF8OtherRegs) * 128 <= kF8LaunchRegs * kF8Threads,
               "register split exceeds the launch");
-constexpr float kPHeadroom = 8.0f;   // P = 2^(y - M + 8): the row's largest entry is 2^8
+constexpr float kRescaleTau = 4.0f;                // M moves when a row maximum exceeds it by more than this
+constexpr float kPHeadroom = 8.0f - kRescaleTau;   // P = 2^(y - M + 4) <= 2^8 < 448
 
 template <int D>
 struct F8Cfg {
@@ -297,7 +301,8 @@ __global__ void __launch_bounds__(kF8Threads, 1)
       float sk = __ldg(k_scale + sbase);   // block 0; the next block's scales are fetched a step ahead
       float sv = __ldg(v_scale + sbase);
       float m = -INFINITY;
-      float l = 0.f;
+      float l = 0.f;    // sum of P as computed: lse
+      float lr = 0.f;   // the same with each block's largest P as rounded: divides O
       bool ok = true;
       for (int j = 0; j < n; ++j, ++c) {
         const float cj = cq * sk;
@@ -334,8 +339,8 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         for (int i = 0; i < 8; ++i) m3[i] = fmaxf(m3[i], s[120 + i]);
         const float mx = fmax3(fmax3(m3[0], m3[1], m3[2]), fmax3(m3[3], m3[4], m3[5]), fmaxf(m3[6], m3[7]));
         const float ymax = mx * cj + vj;
-        const float m_new = fmaxf(m, ymax);
-        const float alpha = ex2_approx(m - m_new);   // 1 when the maximum did not move; 0 on the first block
+        const float m_new = (ymax > m + kRescaleTau) ? ymax : m;
+        const float alpha = (m_new == m) ? 1.0f : ex2_approx(m - m_new);   // 0 on the first block
         const uint64_t c2 = f2_pack(cj, cj);
         const float off = vj + kPHeadroom - m_new;
         const uint64_t off2 = f2_pack(off, off);
@@ -373,7 +378,11 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         float a0, a1, b0, b1;
         f2_unpack(fadd2(acc[0], acc[1]), a0, a1);
         f2_unpack(fadd2(acc[2], acc[3]), b0, b1);
-        l = l * alpha + ((a0 + a1) + (b0 + b1)) * ex2_approx(-vj);
+        const float rowsum = (a0 + a1) + (b0 + b1);
+        const float pmax = ex2_approx(fmaf(mx, cj, off));   // the block's largest P, bit for bit
+        const float inv_sv = ex2_approx(-vj);
+        l = l * alpha + rowsum * inv_sv;
+        lr = lr * alpha + (rowsum + (round_e4m3(pmax) - pmax)) * inv_sv;
         m = m_new;
         tc_fence_before();
         mbar_arrive(bar(C::kPFull + t));
@@ -383,7 +392,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
       if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kOFull + t), e & 1, ctl, 0xb03))) break;
       ++e;
       tc_fence_after();
-      const float inv_l = 1.0f / l;
+      const float inv_l = 1.0f / lr;
       uint8_t* orow = reinterpret_cast<uint8_t*>(out) + ((size_t)ti.bh * N + row) * (D * 2);
 #pragma unroll
       for (int q = 0; q < D / 32; ++q) {

@@ -358,6 +358,16 @@ __device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float 
   return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
+// x rounded to E4M3 (nearest even, saturating) and widened back to float: the value an
+// E4M3 operand built from x holds
+__device__ __forceinline__ float round_e4m3(float x) {
+  uint16_t c;
+  uint32_t h2;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c) : "f"(0.0f), "f"(x));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
+}
+
 template <int DT>
 __device__ __forceinline__ float2 unpack2(uint32_t w) {
   float2 f;

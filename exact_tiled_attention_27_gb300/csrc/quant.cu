@@ -7,13 +7,14 @@
 // block; incoherent processing multiplies Q and K by one fixed random rotation before
 // rounding, spreading an outlier over every dimension without changing any dot product.
 //
-// Three launches, one (head, 128-row block) per CTA and one row per thread:
-//   quant_amax_kernel   the block's rows (rotated when signs are given) and their
-//                       largest magnitude, written to scales[] for the moment
-//   quant_scale_kernel  per head: scale = amax / 448 (the head's largest amax for every
-//                       block when per_tensor), 1 when amax = 0
-//   quant_codes_kernel  code = E4M3(x * (1 / scale)), row-major, or transposed to
-//                       (d, Nt) rows of keys for the V^T operand of the P.V product
+// One (head, 128-row block) per CTA and one row per thread.  With one scale per block
+// a single launch does everything (quant_codes_kernel<FUSED>): the block's rows
+// (rotated when signs are given) stay in registers while the CTA reduces their largest
+// magnitude, then scale = amax / 448 (1 when amax = 0) and code = E4M3(x * (1 / scale)),
+// written row-major, or transposed to (d, Nt) rows of keys for the V^T operand of the
+// P.V product.  One scale per tensor needs the head's largest magnitude first, so that
+// mode runs three launches: quant_amax_kernel (block amax into scales[]),
+// quant_scale_kernel (the head's amax / 448 into every block), quant_codes_kernel.
 // The rotation is x -> x diag(signs) H / sqrt(d) with H the Sylvester-Hadamard matrix,
 // evaluated by the radix-2 butterflies h = 1, 2, 4, ... in float32.  Every rounding
 // step is a fixed round-to-nearest operation, so the codes are reproducible bit for bit.
@@ -64,11 +65,23 @@ __device__ __forceinline__ void load_row(const uint16_t* __restrict__ x, size_t 
   }
 }
 
+// The block's largest magnitude, reduced over the CTA and returned to every thread.
+__device__ __forceinline__ float block_amax(float m) {
+  __shared__ float part[kQRows / 32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = m;
+  __syncthreads();
+  float b = part[0];
+#pragma unroll
+  for (int w = 1; w < kQRows / 32; ++w) b = fmaxf(b, part[w]);
+  return b;
+}
+
 template <int D, int DT, bool ROT>
 __global__ void __launch_bounds__(kQRows) quant_amax_kernel(const uint16_t* __restrict__ x,
                                                             const float* __restrict__ signs,
                                                             float* __restrict__ amax, int N, int nb) {
-  __shared__ float part[kQRows / 32];
   const int bh = blockIdx.x / nb;
   const int blk = blockIdx.x - bh * nb;
   const int r = blk * kQRows + threadIdx.x;
@@ -79,16 +92,8 @@ __global__ void __launch_bounds__(kQRows) quant_amax_kernel(const uint16_t* __re
 #pragma unroll
     for (int i = 0; i < D; ++i) m = fmaxf(m, fabsf(y[i]));
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = m;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float b = part[0];
-#pragma unroll
-    for (int w = 1; w < kQRows / 32; ++w) b = fmaxf(b, part[w]);
-    amax[blockIdx.x] = b;
-  }
+  const float b = block_amax(m);
+  if (threadIdx.x == 0) amax[blockIdx.x] = b;
 }
 
 // One warp per head; turns the block amax values into scales in place.
@@ -109,19 +114,34 @@ __global__ void __launch_bounds__(256) quant_scale_kernel(float* __restrict__ sc
   }
 }
 
-template <int D, int DT, bool ROT, bool TR>
+// FUSED: compute and write the block's scale here (one scale per block); otherwise read
+// it from scales[].
+template <int D, int DT, bool ROT, bool TR, bool FUSED>
 __global__ void __launch_bounds__(kQRows) quant_codes_kernel(const uint16_t* __restrict__ x,
                                                              const float* __restrict__ signs,
-                                                             const float* __restrict__ scales,
+                                                             float* __restrict__ scales,
                                                              uint8_t* __restrict__ x8, int N, int nb, int Nt) {
   const int bh = blockIdx.x / nb;
   const int blk = blockIdx.x - bh * nb;
   const int r = blk * kQRows + threadIdx.x;
-  const float inv = __frcp_rn(scales[blockIdx.x]);
+  float y[D];
+  if (r < N) load_row<D, DT, ROT>(x, (size_t)bh * N + r, signs, y);
+  float scale;
+  if constexpr (FUSED) {
+    float m = 0.f;
+    if (r < N) {
+#pragma unroll
+      for (int i = 0; i < D; ++i) m = fmaxf(m, fabsf(y[i]));
+    }
+    const float amax = block_amax(m);
+    scale = amax > 0.f ? __fdiv_rn(amax, kE4M3Max) : 1.0f;
+    if (threadIdx.x == 0) scales[blockIdx.x] = scale;
+  } else {
+    scale = scales[blockIdx.x];
+  }
+  const float inv = __frcp_rn(scale);
   uint32_t w[D / 4];
   if (r < N) {
-    float y[D];
-    load_row<D, DT, ROT>(x, (size_t)bh * N + r, signs, y);
 #pragma unroll
     for (int q = 0; q < D / 4; ++q)
       w[q] = pack4_e4m3(__fmul_rn(y[4 * q], inv), __fmul_rn(y[4 * q + 1], inv), __fmul_rn(y[4 * q + 2], inv),
@@ -161,6 +181,14 @@ cudaError_t launch_quant_t(const QuantArgs& a, cudaStream_t stream) {
   const int nb = (a.N + kQRows - 1) / kQRows;
   const unsigned grid = (unsigned)((size_t)a.BH * nb);
   const uint16_t* x = static_cast<const uint16_t*>(a.x);
+  uint8_t* x8 = static_cast<uint8_t*>(a.x8);
+  if (!a.per_tensor) {
+    if (a.transpose)
+      quant_codes_kernel<D, DT, ROT, true, true><<<grid, kQRows, 0, stream>>>(x, a.signs, a.scales, x8, a.N, nb, a.Nt);
+    else
+      quant_codes_kernel<D, DT, ROT, false, true><<<grid, kQRows, 0, stream>>>(x, a.signs, a.scales, x8, a.N, nb, a.Nt);
+    return cudaGetLastError();
+  }
   quant_amax_kernel<D, DT, ROT><<<grid, kQRows, 0, stream>>>(x, a.signs, a.scales, a.N, nb);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -168,11 +196,10 @@ cudaError_t launch_quant_t(const QuantArgs& a, cudaStream_t stream) {
   quant_scale_kernel<<<sgrid, 256, 0, stream>>>(a.scales, a.BH, nb, a.per_tensor);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  uint8_t* x8 = static_cast<uint8_t*>(a.x8);
   if (a.transpose)
-    quant_codes_kernel<D, DT, ROT, true><<<grid, kQRows, 0, stream>>>(x, a.signs, a.scales, x8, a.N, nb, a.Nt);
+    quant_codes_kernel<D, DT, ROT, true, false><<<grid, kQRows, 0, stream>>>(x, a.signs, a.scales, x8, a.N, nb, a.Nt);
   else
-    quant_codes_kernel<D, DT, ROT, false><<<grid, kQRows, 0, stream>>>(x, a.signs, a.scales, x8, a.N, nb, a.Nt);
+    quant_codes_kernel<D, DT, ROT, false, false><<<grid, kQRows, 0, stream>>>(x, a.signs, a.scales, x8, a.N, nb, a.Nt);
   return cudaGetLastError();
 }
 

@@ -158,6 +158,12 @@ EXTRA_WORKLOADS = {
     # block-sparse (butterfly) training step at long sequence length
     "x5_butterfly_64k": dict(kind="sparse", B=1, H=16, Hkv=16, Nq=65536, Nk=65536, d=64, dtype="bf16",
                              causal=False, backward=True, index=24),
+    # FP8 (E4M3) forward at the shapes of the 16-bit c4a / c4b workloads: Q and K rotated
+    # and block-quantized, V block-quantized into the transposed layout
+    "x6_fp8_c4a": dict(kind="fp8", B=4, H=16, Hkv=16, Nq=8192, Nk=8192, d=64, dtype="bf16", causal=True,
+                       backward=False, index=25),
+    "x7_fp8_c4b": dict(kind="fp8", B=4, H=8, Hkv=8, Nq=8192, Nk=8192, d=128, dtype="bf16", causal=True,
+                       backward=False, index=26),
 }
 
 

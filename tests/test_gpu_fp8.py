@@ -102,6 +102,28 @@ def test_fp8_forward_matches_oracle(B, H, N, d, dtype, causal, rotate):
     G.check_forward_fp8(G.to_f64(o), G.to_f64(lse), o_ref, lse_ref, vmax, f"fp8 B{B} H{H} N{N} d{d} causal={causal}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_rows_dominated_by_one_key_return_its_value(d):
+    """K = Q with large entries: every causal row's own key outweighs the others by
+    e^40 or more, so O_i = V_i.  The dominant weight's E4M3 rounding (up to 2^-4) must
+    not reach O: the kernel divides by the weight P.V actually used."""
+    N = 640
+    c = make_case(1, 2, N, d, "bf16", True, workload_index=234, length_index=d)
+    q64 = bits_to_f64(c.q, "bf16") * 5.0
+    cq, sq = F.quantize_blocks(q64)
+    cv, sv = F.quantize_blocks(bits_to_f64(c.v, "bf16"))
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    o, lse = forward_fp8(dev(cq), dev(cq), dev(_vt_layout(cv)), dev(sq), dev(sq), dev(sv), causal=True)
+    torch.cuda.synchronize()
+    assert last_kernel_status() == 0
+    o_ref, lse_ref = F.attn_fp8_ref(cq, sq, cq, sq, cv, sv, d ** -0.5, True)
+    v_deq = F.dequantize_blocks(cv, sv)
+    assert np.abs(o_ref - v_deq).max() < 1e-12          # the reference is V itself
+    err = np.abs(G.to_f64(o) - o_ref)
+    assert np.all(err <= 2.0 ** -8 * np.abs(o_ref) + 1e-6), f"max err {err.max():.3e}"
+    assert G.maxabs(G.to_f64(lse), lse_ref) <= G.LSE_ABS
+
+
 def _fp8_error(q_bits, k_bits, v_bits, scale, causal, per_tensor, signs):
     """relL2 of the FP8 path's O (GPU quantizer + FP8 forward) against exact attention
     on the original 16-bit inputs."""
