@@ -250,28 +250,64 @@ def run_ours(args, w, rank, world, local_rank):
     # ---------------------------------------------------------------- end to end (host buffers)
     e2e = None
     if args.e2e_steps > 0:
-        h_out = [torch.empty_like(o, device="cpu").pin_memory(), torch.empty_like(lse, device="cpu").pin_memory()]
-        if w["backward"]:
-            h_out += [torch.empty_like(q, device="cpu").pin_memory() for _ in range(3)]
-        d_out = [o, lse] + ([dq, dk, dv] if w["backward"] else [])
+        # Every step uploads its inputs from pinned host memory and reads all of its
+        # outputs back, as a training loop's data path does.  The steps are pipelined on
+        # three streams with double-buffered device tensors: step i+1's upload and step
+        # i-1's read-back run while step i computes (the copy engines are full duplex).
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        h_out = [[torch.empty_like(o, device="cpu").pin_memory(), torch.empty_like(lse, device="cpu").pin_memory()]
+                 + ([torch.empty_like(q, device="cpu").pin_memory() for _ in range(3)] if w["backward"] else [])
+                 for _ in range(2)]
+        dbuf_in = [d_in, [torch.empty_like(t) for t in d_in]]
+        dbuf_out = [[o, lse] + ([dq, dk, dv] if w["backward"] else []),
+                    [torch.empty_like(o), torch.empty_like(lse)]
+                    + ([torch.empty_like(q) for _ in range(3)] if w["backward"] else [])]
         h2d = sum(t.numel() * t.element_size() for t in h_in)
-        d2h = sum(t.numel() * t.element_size() for t in h_out)
+        d2h = sum(t.numel() * t.element_size() for t in h_out[0])
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_comp = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
+        for e in ev_comp + ev_out:
+            e.record(stream)
+        sh_c = fa._stream_handle(stream)
+
+        def compute(b):
+            qi, ki, vi = dbuf_in[b][:3]
+            oo, ll = dbuf_out[b][:2]
+            call(lib.fa_fwd(P(qi), P(ki), P(vi), P(oo), P(ll), B, H, N, d, scale, causal, dcode, sh_c), "fa_fwd")
+            if w["backward"]:
+                gq, gk, gv = dbuf_out[b][2:]
+                for fn in stages:
+                    call(fn(P(qi), P(ki), P(vi), P(oo), P(dbuf_in[b][3]), P(ll), P(gq), P(gk), P(gv), P(ws), ws_bytes,
+                            B, H, N, d, scale, causal, dcode, sh_c), fn.__name__)
+
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        for it in range(args.e2e_steps + 2):
+        total = args.e2e_steps + 2
+        for it in range(total):
+            b = it % 2
             if it == 2:
-                e0.record(stream)
-            for hsrc, ddst in zip(h_in, d_in):
-                ddst.copy_(hsrc, non_blocking=True)
-            fwd()
-            for fn in stages:
-                call(fn(*bwd_args()), fn.__name__)
-            for dsrc, hdst in zip(d_out, h_out):
-                hdst.copy_(dsrc, non_blocking=True)
-        e1.record(stream)
+                e0.record(s_in)
+            with torch.cuda.stream(s_in):          # upload step it (after step it-2 used the buffer)
+                s_in.wait_event(ev_comp[b])
+                for hsrc, ddst in zip(h_in, dbuf_in[b]):
+                    ddst.copy_(hsrc, non_blocking=True)
+                ev_in[b].record(s_in)
+            stream.wait_event(ev_in[b])            # compute step it (after step it-2's outputs were read)
+            stream.wait_event(ev_out[b])
+            compute(b)
+            ev_comp[b].record(stream)
+            with torch.cuda.stream(s_out):         # read back step it
+                s_out.wait_event(ev_comp[b])
+                for dsrc, hdst in zip(dbuf_out[b], h_out[b]):
+                    hdst.copy_(dsrc, non_blocking=True)
+                ev_out[b].record(s_out)
+        e1.record(s_out)
         torch.cuda.synchronize()
         t_e2e = e0.elapsed_time(e1) / args.e2e_steps
         e2e = {"value": round(world * f_step / (t_e2e * 1e-3) / 1e12, 3), "unit": UNIT,
-               "ms_per_step": round(t_e2e, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+               "ms_per_step": round(t_e2e, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "pipelining": "step i+1 upload and step i-1 read-back overlap step i's kernels (3 streams, "
+                             "double-buffered device tensors)"}
 
     # dominant kernel: the dK/dV kernel when there is a backward, else the forward
     if w["backward"]:
