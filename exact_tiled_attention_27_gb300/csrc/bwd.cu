@@ -371,8 +371,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             __syncwarp();
           }
           if (!wait_warp(bar(C::kDSFull), s & 1, ctl, 0x507) ||
-              (i == 0 && it > 0 && !wait_warp(bar(C::kDKVEmpty), (it - 1) & 1, ctl, 0x508)) ||
-              (C::kEarly && s > 0 && !wait_warp(bar(C::kDQFree), (s - 1) & 1, ctl, 0x509))) {
+              (i == 0 && it > 0 && !wait_warp(bar(C::kDKVEmpty), (it - 1) & 1, ctl, 0x508))) {
             ok = false;
             break;
           }
@@ -380,10 +379,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (elect_one()) {
             const uint32_t qbase = qaddr(s), obase = oaddr(s);
             const uint64_t dsk = sdesc_sw128(dst, 16, 1024);                 // dS^T, K-major (A of dK)
-            const uint64_t dsmn = sdesc_sw128(dst, kChunkBytes, 1024);       // dS, MN-major (A of dQ)
             const uint64_t omn = sdesc_sw128(obase, kChunkBytes, 1024);      // dO, MN-major (B of dV)
             const uint64_t qmn = sdesc_sw128(qbase, kChunkBytes, 1024);      // Q, MN-major (B of dK)
-            const uint64_t kmn = sdesc_sw128(kbase, kChunkBytes, 1024);      // K, MN-major (B of dQ)
 #pragma unroll
             for (int kk = 0; kk < kRows / 16; ++kk) {
               const uint32_t acc = (i == 0 && kk == 0) ? 0u : 1u;
@@ -394,6 +391,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               const uint32_t aoff = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
               umma_ss(tmem + C::kTmDK, dsk + aoff, qmn + rows16, idesc_kv, acc);
             }
+          }
+          __syncwarp();
+          // d = 64: dQ has its own columns, which the dQ warpgroup must have read out for
+          // the previous block; dV and dK above did not wait for that (at a tile's first
+          // block the same warpgroup is also writing the previous tile's dK and dV)
+          if (C::kEarly && s > 0 && !wait_warp(bar(C::kDQFree), (s - 1) & 1, ctl, 0x509)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (elect_one()) {
+            const uint64_t dsmn = sdesc_sw128(dst, kChunkBytes, 1024);       // dS, MN-major (A of dQ)
+            const uint64_t kmn = sdesc_sw128(kbase, kChunkBytes, 1024);      // K, MN-major (B of dQ)
 #pragma unroll
             for (int kk = 0; kk < kRows / 16; ++kk) {
               // dQ = dS K: A = dS (q x keys) read MN-major from the dS^T block; B = K MN-major
