@@ -15,14 +15,17 @@
 //   * operands: Q and K tiles are 128 rows of d bytes (64-byte swizzle at d = 64,
 //     128-byte at d = 128).  V is stored transposed, V^T with one row of keys per
 //     channel, so that the B operand of P.V is K-major like every other 8-bit operand.
+//     P is the A operand from tensor memory, four E4M3 codes per column over the first
+//     32 columns of S_t (S_t(j+1) is issued after P_t(j).V by the same thread, and the
+//     tensor core runs them in that order).
 //   * scales: block j of K scales S by sk_j, and the query block by sq, so the exponent
 //     uses c_j = scale * log2(e) * sq * sk_j.  The scale sv_j of V block j is folded
 //     into that block's probabilities before they are rounded: the kernel works with
 //     y = s c_j + log2(sv_j), so P.V needs no per-block rescale of O, and the running
 //     sum l adds the same probabilities divided by sv_j.
-//   * P: rounded to E4M3 and written to shared memory (128 x 128 bytes, 128-byte
-//     swizzle, K-major A operand).  The running maximum M only moves when a row
-//     maximum exceeds it by more than 4 (base 2), and P is formed as 2^(y - M + 4), so
+//   * P: rounded to E4M3 and written back to tensor memory.  The running maximum M
+//     only moves when a row maximum exceeds it by more than 4 (base 2), and P is
+//     formed as 2^(y - M + 4), so
 //     P <= 2^8 stays below E4M3's 448 and entries down to 2^-13 of a row's largest
 //     stay representable; O is rescaled only on the rare steps where M moves.
 //   * sums: l adds the unrounded P (lse = (M - 4 + log2 l) ln 2); lr, which divides O,
@@ -50,14 +53,12 @@ constexpr float kPHeadroom = 8.0f - kRescaleTau;   // P = 2^(y - M + 4) <= 2^8 <
 template <int D>
 struct F8Cfg {
   static constexpr int kTileBytes = kTileRows * D;          // Q, K: 128 rows x d bytes; V^T: d rows x 128 bytes
-  static constexpr int kPBytes = kTileRows * kTileRows;     // P of one sub-tile
   static constexpr int kQBufs = (D == 64) ? 2 : 1;
   static constexpr int kStages = (D == 64) ? 6 : 4;
   static constexpr int kOffQ = 0;                           // [kQBufs][2 sub-tiles]
   static constexpr int kOffK = kOffQ + kQBufs * 2 * kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffP = kOffV + kStages * kTileBytes;   // [2 sub-tiles]
-  static constexpr int kOffBar = kOffP + 2 * kPBytes;
+  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
   static constexpr int kQFull = 0;
   static constexpr int kQEmpty = kQFull + kQBufs;
   static constexpr int kKFull = kQEmpty + kQBufs;
@@ -71,6 +72,7 @@ struct F8Cfg {
   static constexpr int kNumBars = kDrain + 1;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory");
+  // P_t (E4M3, four per column) occupies the first 32 columns of S_t
   __host__ __device__ static constexpr uint32_t tm_s(int t) { return t * 128; }
   __host__ __device__ static constexpr uint32_t tm_o(int t) { return 256 + t * 128; }
 };
@@ -251,11 +253,11 @@ __global__ void __launch_bounds__(kF8Threads, 1)
           }
           tc_fence_after();
           if (elect_one()) {
-            const uint32_t pbase = smem_u32(smem + C::kOffP + t * C::kPBytes);
 #pragma unroll
-            for (int kk = 0; kk < kTileRows / 32; ++kk)   // O += P V: A = P (rows x keys), B = V^T (d x keys)
-              umma_ss_f8(tmem + C::tm_o(t), sdesc_sw128(pbase + kk * 32, 16, 1024),
-                         sdesc_sw128(vbase + kk * 32, 16, 1024), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kTileRows / 32; ++kk)   // O += P V: A = P from tensor memory (32 keys = 8
+                                                          // columns), B = V^T (d x keys)
+              umma_ts_f8(tmem + C::tm_o(t), tmem + C::tm_s(t) + kk * 8, sdesc_sw128(vbase + kk * 32, 16, 1024),
+                         idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
             if (j + 1 < n[t]) {
               issue_s(t, qbase0 + t * C::kTileBytes, knext);
               umma_commit(bar(C::kSFull + t));
@@ -286,7 +288,6 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t s_addr = tmem + lane_base + C::tm_s(t);
     const uint32_t o_addr = tmem + lane_base + C::tm_o(t);
-    uint8_t* prow = smem + C::kOffP + t * C::kPBytes;
     uint32_t c = 0;
     uint32_t e = 0;
     for (int k = 0, tile = persistent_tile(0); tile < ntiles; tile = persistent_tile(++k)) {
@@ -355,12 +356,8 @@ __global__ void __launch_bounds__(kF8Threads, 1)
           acc[q & 3] = fadd2(acc[q & 3], fadd2(f2_pack(p0, p1), f2_pack(p2, p3)));
           pk[q] = pack4_e4m3(p0, p1, p2, p3);
         }
-        // P row into the 128-byte-swizzled K-major tile: 16-byte unit u of row tid
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(prow + tid * 128 + ((u ^ (tid & 7)) << 4)) =
-              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-        fence_proxy_async_smem();
+        // P (four E4M3 codes per column) over the first 32 columns of S_t
+        tmem_st32(s_addr, pk);
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
           // O holds every earlier P.V (committed before this S): bring it to the new maximum
 #pragma unroll
@@ -384,6 +381,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         l = l * alpha + rowsum * inv_sv;
         lr = lr * alpha + (rowsum + (round_e4m3(pmax) - pmax)) * inv_sv;
         m = m_new;
+        tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar(C::kPFull + t));
       }
