@@ -54,7 +54,7 @@ template <int D>
 struct F8Cfg {
   static constexpr int kTileBytes = kTileRows * D;          // Q, K: 128 rows x d bytes; V^T: d rows x 128 bytes
   static constexpr int kQBufs = (D == 64) ? 2 : 1;
-  static constexpr int kStages = (D == 64) ? 6 : 4;
+  static constexpr int kStages = (D == 64) ? 8 : 6;
   static constexpr int kOffQ = 0;                           // [kQBufs][2 sub-tiles]
   static constexpr int kOffK = kOffQ + kQBufs * 2 * kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
