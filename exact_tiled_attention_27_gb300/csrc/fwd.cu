@@ -109,7 +109,7 @@ template <int D, int DT, bool CAUSAL, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, uint16_t* __restrict__ out, float* __restrict__ lse,
-               int BH, int H, int G, int Nq, int Nk, float scale_log2, int balanced, unsigned int* err_word,
+               int BH, int H, int G, int Nq, int Nk, float scale_log2, int pairing, unsigned int* err_word,
                uint64_t limit_ns) {
   using C = FwdCfg<D>;
   constexpr bool GEN = MODE == 1;
@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // address, descriptor and loop bound derived from it) as warp-uniform
   const int warp = __shfl_sync(0xffffffffu, threadIdx.x >> 5, 0);
   const int nqb = (Nq + kTileRows - 1) / kTileRows;
-  const int ntiles = BH * ((nqb + 1) >> 1);
+  const int ntiles = forward_tiles(BH, nqb, pairing);
   // key block of step j of tile ti: j, or the j-th block of the pair's butterfly list
   auto key_block = [&](const TileInfo& ti, int j) {
     return SPARSE ? bfly_block(ti.qb0 >> 1, j, (nqb + 1) >> 1, CAUSAL ? -1 : 0, 0) : j;
@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0;
       bool ok = true;
       for (int k = 0, tile = persistent_tile(0); ok && tile < ntiles; tile = persistent_tile(++k), ++it) {
-        const TileInfo ti = decode_tile<MODE>(tile, BH, H, G, Nq, Nk, CAUSAL, balanced != 0);
+        const TileInfo ti = decode_tile<MODE>(tile, BH, H, G, Nq, Nk, CAUSAL, pairing);
         const int qbuf = it % C::kQBufs;
         if (it >= C::kQBufs && !wait_warp(bar(C::kQEmpty + qbuf), ((it / C::kQBufs) - 1) & 1, ctl, 0x101)) {
           ok = false;
@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       for (int k = 0, tile = persistent_tile(0); ok && tile < ntiles; tile = persistent_tile(++k), ++it) {
-        const TileInfo ti = decode_tile<MODE>(tile, BH, H, G, Nq, Nk, CAUSAL, balanced != 0);
+        const TileInfo ti = decode_tile<MODE>(tile, BH, H, G, Nq, Nk, CAUSAL, pairing);
         const int n[2] = {ti.n0, ti.n1};
         const int qbuf = it % C::kQBufs;
         const uint32_t qbase0 = smem_u32(smem + C::kOffQ + (qbuf * 2) * C::kTileBytes);
@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t c = 0;   // steps of this sub-tile (S-full / P-full phases)
     uint32_t e = 0;   // epilogues of this sub-tile
     for (int k = 0, tile = persistent_tile(0); tile < ntiles; tile = persistent_tile(++k)) {
-      const TileInfo ti = decode_tile<MODE>(tile, BH, H, G, Nq, Nk, CAUSAL, balanced != 0);
+      const TileInfo ti = decode_tile<MODE>(tile, BH, H, G, Nq, Nk, CAUSAL, pairing);
       const int n = t == 0 ? ti.n0 : ti.n1;
       const int qb = t == 0 ? ti.qb0 : ti.qb1;
       const int row = qb * kTileRows + tid;
@@ -531,13 +531,11 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   e = cudaFuncGetAttributes(&attr, kern);
   if (e != cudaSuccess) return e;
   if (attr.numRegs * kThreads < (2 * kSoftmaxRegs + kOtherRegs) * 128) return cudaErrorInvalidConfiguration;
-  const int nqb = (a.Nq + kTileRows - 1) / kTileRows;
-  const int ntiles = a.BH * ((nqb + 1) / 2);
-  const int grid = ntiles < a.num_sms ? ntiles : a.num_sms;
   // (the butterfly pattern is defined on adjacent pairs of query blocks)
-  const int balanced = (CAUSAL && MODE != 2) ? choose_balanced_pairing(a.BH, a.Nq, a.Nk, grid) : 0;
+  int grid = 0;
+  const int pairing = choose_pairing(a.BH, a.Nq, a.Nk, CAUSAL, MODE != 2, MODE != 2, a.num_sms, &grid);
   return launch_overlapped(kern, grid, kThreads, C::kSmemBytes, stream, a.tm_q, a.tm_k, a.tm_v,
-                           static_cast<uint16_t*>(a.o), a.lse, a.BH, a.H, a.G, a.Nq, a.Nk, a.scale_log2, balanced,
+                           static_cast<uint16_t*>(a.o), a.lse, a.BH, a.H, a.G, a.Nq, a.Nk, a.scale_log2, pairing,
                            a.err_word, a.limit_ns);
 }
 

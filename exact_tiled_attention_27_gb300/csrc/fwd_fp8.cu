@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     fwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_vt, const float* __restrict__ q_scale,
                    const float* __restrict__ k_scale, const float* __restrict__ v_scale, uint16_t* __restrict__ out,
-                   float* __restrict__ lse, int BH, int N, float scale_log2, int balanced, unsigned int* err_word,
+                   float* __restrict__ lse, int BH, int N, float scale_log2, int pairing, unsigned int* err_word,
                    uint64_t limit_ns) {
   using C = F8Cfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
 
   const int warp = __shfl_sync(0xffffffffu, threadIdx.x >> 5, 0);
   const int nqb = (N + kTileRows - 1) / kTileRows;
-  const int ntiles = BH * ((nqb + 1) >> 1);
+  const int ntiles = forward_tiles(BH, nqb, pairing);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kQBufs; ++i) {
@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     int it = 0;
     bool ok = true;
     for (int k = 0, tile = persistent_tile(0); ok && tile < ntiles; tile = persistent_tile(++k), ++it) {
-      const TileInfo ti = decode_tile<0>(tile, BH, 1, 1, N, N, CAUSAL, balanced != 0);
+      const TileInfo ti = decode_tile<0>(tile, BH, 1, 1, N, N, CAUSAL, pairing);
       const int qbuf = it % C::kQBufs;
       if (it >= C::kQBufs && !wait_warp(bar(C::kQEmpty + qbuf), ((it / C::kQBufs) - 1) & 1, ctl, 0x901)) {
         ok = false;
@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                    kk > 0 ? 1u : 0u);
     };
     for (int k = 0, tile = persistent_tile(0); ok && tile < ntiles; tile = persistent_tile(++k), ++it) {
-      const TileInfo ti = decode_tile<0>(tile, BH, 1, 1, N, N, CAUSAL, balanced != 0);
+      const TileInfo ti = decode_tile<0>(tile, BH, 1, 1, N, N, CAUSAL, pairing);
       const int n[2] = {ti.n0, ti.n1};
       const int qbuf = it % C::kQBufs;
       const uint32_t qbase0 = smem_u32(smem + C::kOffQ + (qbuf * 2) * C::kTileBytes);
@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     uint32_t c = 0;
     uint32_t e = 0;
     for (int k = 0, tile = persistent_tile(0); tile < ntiles; tile = persistent_tile(++k)) {
-      const TileInfo ti = decode_tile<0>(tile, BH, 1, 1, N, N, CAUSAL, balanced != 0);
+      const TileInfo ti = decode_tile<0>(tile, BH, 1, 1, N, N, CAUSAL, pairing);
       const int n = t == 0 ? ti.n0 : ti.n1;
       if (n == 0) continue;
       const int qb = t == 0 ? ti.qb0 : ti.qb1;
@@ -432,13 +432,11 @@ cudaError_t launch_fp8_t(const FwdF8Args& a, cudaStream_t stream) {
   e = cudaFuncGetAttributes(&attr, kern);
   if (e != cudaSuccess) return e;
   if (attr.numRegs * kF8Threads < (2 * kF8SoftmaxRegs + kF8OtherRegs) * 128) return cudaErrorInvalidConfiguration;
-  const int nqb = (a.N + kTileRows - 1) / kTileRows;
-  const int ntiles = a.BH * ((nqb + 1) / 2);
-  const int grid = ntiles < a.num_sms ? ntiles : a.num_sms;
-  const int balanced = CAUSAL ? choose_balanced_pairing(a.BH, a.N, a.N, grid) : 0;
+  int grid = 0;
+  const int pairing = choose_pairing(a.BH, a.N, a.N, CAUSAL, true, true, a.num_sms, &grid);
   return launch_overlapped(kern, grid, kF8Threads, C::kSmemBytes, stream, a.tm_q, a.tm_k, a.tm_vt, a.q_scale,
                            a.k_scale, a.v_scale, static_cast<uint16_t*>(a.o), a.lse, a.BH, a.N, a.scale_log2,
-                           balanced, a.err_word, a.limit_ns);
+                           pairing, a.err_word, a.limit_ns);
 }
 
 }  // namespace

@@ -40,23 +40,29 @@ __host__ __device__ __forceinline__ int visible_kv_blocks(int qb, int Nq, int Nk
 }
 
 // Work tile `tile` -> head, the two query blocks and their key/value block counts
-// (n1 = 0 when there is no second block).  Two pairings of the query blocks:
-//   adjacent  (2p, 2p+1): the two sub-tiles share every key/value block; pairs are
-//             numbered heaviest first under the causal mask.
-//   balanced  (i, nqb-1-i): under the causal mask every pair costs nqb+1 blocks, which
-//             evens out the work when there are only about as many pairs as SMs.
+// (n1 = 0 when there is no second block).  Three pairings of the query blocks:
+//   0 adjacent  (2p, 2p+1): the two sub-tiles share every key/value block; pairs are
+//               numbered heaviest first under the causal mask.
+//   1 balanced  (i, nqb-1-i): under the causal mask every pair costs nqb+1 blocks, which
+//               evens out the work when there are only about as many pairs as SMs.
+//   2 single    one query block per tile, heaviest first: for launches with fewer pairs
+//               than SMs, so that every SM works and a lone softmax warpgroup runs
+//               without the other's contention.
 // MODE: 0 plain (Nq = Nk, one key/value head per query head), 1 general (fa_fwd_cross),
 // 2 butterfly block pattern (fa_fwd_sparse).
 template <int MODE>
 __device__ __forceinline__ TileInfo decode_tile(int tile, int BH, int H, int G, int Nq, int Nk, bool causal,
-                                                bool balanced) {
+                                                int pairing) {
   const int nqb = (Nq + kTileRows - 1) / kTileRows;
   const int npairs = (nqb + 1) >> 1;
   TileInfo ti;
   const int r = tile / BH;
   ti.bh = tile - r * BH;
   ti.kvh = MODE == 1 ? (ti.bh / H) * (H / G) + (ti.bh % H) / G : ti.bh;
-  if (balanced) {
+  if (pairing == 2) {
+    ti.qb0 = nqb - 1 - r;
+    ti.qb1 = nqb;   // none
+  } else if (pairing == 1) {
     ti.qb0 = r;
     ti.qb1 = nqb - 1 - r;
   } else {
@@ -85,6 +91,31 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, int BH, int H, int G, 
 // CTAs and keep the one whose busiest CTA has less work (adjacent on ties, since its
 // sub-tiles share more key/value loads).  With many tiles per CTA both balance well,
 // so the simulation is only run for small launches.
+// Tiles of a launch with this pairing.
+__host__ __device__ __forceinline__ int forward_tiles(int BH, int nqb, int pairing) {
+  return BH * (pairing == 2 ? nqb : (nqb + 1) >> 1);
+}
+
+// Pairing of a launch: single query blocks when there are fewer pairs than SMs (and the
+// pattern allows it), else adjacent pairs or, under the causal mask, balanced ones when
+// their snake schedule is lighter (choose_balanced_pairing).
+int choose_balanced_pairing(int BH, int Nq, int Nk, int grid);
+inline int choose_pairing(int BH, int Nq, int Nk, bool causal, bool allow_single, bool allow_balanced,
+                          int num_sms, int* grid) {
+  const int nqb = (Nq + kTileRows - 1) / kTileRows;
+  const int pairs = forward_tiles(BH, nqb, 0);
+  int pairing = 0;
+  if (allow_single && nqb > 1 && pairs < num_sms) {
+    pairing = 2;
+  } else if (causal && allow_balanced) {
+    const int g = pairs < num_sms ? pairs : num_sms;
+    pairing = choose_balanced_pairing(BH, Nq, Nk, g);
+  }
+  const int tiles = forward_tiles(BH, nqb, pairing);
+  *grid = tiles < num_sms ? tiles : num_sms;
+  return pairing;
+}
+
 int choose_balanced_pairing(int BH, int Nq, int Nk, int grid) {
   const int nqb = (Nq + kTileRows - 1) / kTileRows;
   const int npairs = (nqb + 1) / 2;
