@@ -82,6 +82,8 @@ FWD_CASES = [
     (1, 3, 130, 64, "bf16", True, False),
     (1, 2, 4096, 64, "fp16", True, False),
     (1, 1, 100, 128, "bf16", False, False),
+    (2, 2, 1, 64, "bf16", True, True),         # one key: the V^T rows are padded from 1 to 16 bytes
+    (1, 2, 17, 128, "fp16", False, False),     # V^T row stride 32 bytes, 15 of them padding
 ]
 
 
