@@ -64,15 +64,18 @@ struct BwdCfg {
   static constexpr int kTileBytes = kRows * D * 2;
   static constexpr bool kEarly = (D == 64);          // next S^T / dP^T issued before this block's gradients
   static constexpr int kKVBufs = (D == 64) ? 2 : 1;
-  static constexpr int kQBufs = (D == 64) ? 2 : 1;
+  static constexpr int kQBufs = (D == 64) ? 3 : 1;
+  // dQ staging chunks of 128 rows x 32 floats: d = 64 stages its two chunks one after the
+  // other through one buffer, which leaves room for the third Q/dO buffer
+  static constexpr int kDQSChunks = (D == 64) ? 1 : 2;
   static_assert(!kEarly || kQBufs >= 2, "early issue needs two Q/dO buffers");
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kKVBufs * kTileBytes;
   static constexpr int kOffQ = kOffV + kKVBufs * kTileBytes;
   static constexpr int kOffDO = kOffQ + kQBufs * kTileBytes;
   static constexpr int kOffDST = kOffDO + kQBufs * kTileBytes;       // 128 x 128 16-bit, K-major SW128
-  static constexpr int kOffDQS = kOffDST + 2 * kChunkBytes;          // dQ staging: 2 x (128 rows x 32 float), SW128
-  static constexpr int kOffStats = kOffDQS + 2 * kChunkBytes;        // [kQBufs][-lse2[128], -D[128]] float
+  static constexpr int kOffDQS = kOffDST + 2 * kChunkBytes;          // dQ staging: kDQSChunks x (128 rows x 32 float), SW128
+  static constexpr int kOffStats = kOffDQS + kDQSChunks * kChunkBytes;   // [kQBufs][-lse2[128], -D[128]] float
   static constexpr int kOffRing = kOffStats + kQBufs * 2 * kRows * 4;   // int[kTileSlots]
   static constexpr int kOffBar = kOffRing + kTileSlots * 4;
   // barriers
@@ -93,6 +96,7 @@ struct BwdCfg {
   static constexpr int kDrain = kTileEmpty + kTileSlots;
   static constexpr int kNumBars = kDrain + 1;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory");
   // tensor memory columns (512 allocated)
   static constexpr uint32_t kTmST = 0;
   static constexpr uint32_t kTmDPT = 128;
@@ -614,27 +618,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_arrive(bar(C::kDQFree));
           }
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint8_t* box = smem + C::kOffDQS + c * kChunkBytes;
+          for (int c0 = 0; c0 < 2; c0 += C::kDQSChunks) {   // one or two staging rounds
 #pragma unroll
-            for (int v = 0; v < 8; ++v)
-              *reinterpret_cast<uint4*>(box + sw128_offset(u, v)) =
-                  make_uint4(r[c][4 * v], r[c][4 * v + 1], r[c][4 * v + 2], r[c][4 * v + 3]);
-          }
-          fence_proxy_async_smem();
-          named_bar_sync(1, 128);
-          if (warp == 8) {
-            if (elect_one()) {
+            for (int cc = 0; cc < C::kDQSChunks; ++cc) {
+              uint8_t* box = smem + C::kOffDQS + cc * kChunkBytes;
 #pragma unroll
-              for (int c = 0; c < 2; ++c)
-                tma_reduce_add_3d(&tm_dq, smem_u32(smem + C::kOffDQS + c * kChunkBytes), (half * 2 + c) * 32,
-                                  qi * kRows, bhq);
-              bulk_commit_group();
-              bulk_wait_read_all();   // the staging tile may be overwritten after this
+              for (int v = 0; v < 8; ++v)
+                *reinterpret_cast<uint4*>(box + sw128_offset(u, v)) = make_uint4(
+                    r[c0 + cc][4 * v], r[c0 + cc][4 * v + 1], r[c0 + cc][4 * v + 2], r[c0 + cc][4 * v + 3]);
             }
-            __syncwarp();
+            fence_proxy_async_smem();
+            named_bar_sync(1, 128);
+            if (warp == 8) {
+              if (elect_one()) {
+#pragma unroll
+                for (int cc = 0; cc < C::kDQSChunks; ++cc)
+                  tma_reduce_add_3d(&tm_dq, smem_u32(smem + C::kOffDQS + cc * kChunkBytes),
+                                    (half * 2 + c0 + cc) * 32, qi * kRows, bhq);
+                bulk_commit_group();
+                bulk_wait_read_all();   // the staging tile may be overwritten after this
+              }
+              __syncwarp();
+            }
+            named_bar_sync(1, 128);
           }
-          named_bar_sync(1, 128);
         }
       }
       }
