@@ -395,6 +395,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               const uint32_t aoff = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
               umma_ss(tmem + C::kTmDK, dsk + aoff, qmn + rows16, idesc_kv, acc);
             }
+            // d = 128 (one Q/dO buffer): dV and dK are the last readers of this block's Q
+            // and dO, so the producer may refill the buffer while dQ (which reads dS and K)
+            // still runs.  (At d = 64, with three buffers, the earlier refill only competes
+            // with dQ and measured slower.)
+            if constexpr (!C::kEarly) umma_commit(bar(C::kQEmpty + s % C::kQBufs));
           }
           __syncwarp();
           // d = 64: dQ has its own columns, which the dQ warpgroup must have read out for
@@ -415,7 +420,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               umma_ss(tmem + C::kTmDQ, dsmn + rows16, kmn + rows16, idesc_q, kk > 0 ? 1u : 0u);
             }
             umma_commit(bar(C::kMmaDone));
-            umma_commit(bar(C::kQEmpty + s % C::kQBufs));
+            if constexpr (C::kEarly) umma_commit(bar(C::kQEmpty + s % C::kQBufs));
             umma_commit(bar(C::kDQFull));
           }
           __syncwarp();
