@@ -2,7 +2,7 @@
 """Attention throughput on GB300: TFLOPS of the forward and of forward+backward.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--e2e-steps E] [--cpu-seconds S]
+                    [--workload NAME] [--e2e-steps E] [--cpu-seconds S] [--cpu-threads T]
 
 A step is one forward (fa_fwd) and one backward (the three launches of fa_bwd) over
 one batch of seeded synthetic inputs already resident in device memory.  Between
@@ -28,6 +28,23 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
+
+
+def _cpu_threads_arg(argv):
+    """The --cpu-threads value, read before numpy is first imported: the BLAS library
+    fixes its thread pool when it loads."""
+    for i, a in enumerate(argv):
+        if a == "--cpu-threads" and i + 1 < len(argv):
+            return argv[i + 1]
+        if a.startswith("--cpu-threads="):
+            return a.split("=", 1)[1]
+    return None
+
+
+CPU_THREADS = _cpu_threads_arg(sys.argv[1:])
+if CPU_THREADS is not None:
+    for _var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[_var] = CPU_THREADS
 
 from exact_tiled_attention_27_gb300.inputs import EXTRA_WORKLOADS, WORKLOADS, extra_case, workload_case  # noqa: E402
 
@@ -650,6 +667,11 @@ def oracle_sample(w, seconds, max_heads=None):
     return done, el, per_head * done / el / 1e12
 
 
+def oracle_threads():
+    """Threads the oracle's BLAS calls run on: --cpu-threads, else every host core."""
+    return int(CPU_THREADS) if CPU_THREADS is not None else os.cpu_count()
+
+
 _CASE_CACHE = {}
 
 
@@ -672,7 +694,7 @@ def run_reference(args, w):
         heads_total += nh
         el_total += el
     value = statistics.mean(vals)
-    cores = os.cpu_count()
+    cores = oracle_threads()
     sample = (f"{heads_total} whole (b,h) heads of {w['B'] * w['H']} over {args.steps} steps, "
               f"{'forward+backward' if w['backward'] else 'forward'}, float64 numpy, {el_total:.1f} s")
     return {"metric": METRIC, "value": round(value, 6), "unit": UNIT, "impl": "reference", "n_gpus": args.gpus,
@@ -696,7 +718,11 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="wall-clock budget of the oracle's CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-threads", type=int, default=None,
+                    help="BLAS threads of the oracle (default: every host core)")
     args = ap.parse_args()
+    if args.cpu_threads is not None and args.cpu_threads < 1:
+        ap.error("--cpu-threads must be >= 1")
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -726,7 +752,7 @@ def main():
     if rank == 0 and not args.no_cpu_baseline:
         nh, el, tf = oracle_sample(w, args.cpu_seconds)
         result["cpu_baseline"] = {
-            "value": round(tf, 6), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "value": round(tf, 6), "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
             "sample": (f"{nh} whole (b,h) heads of {w['B'] * w['H']}, "
                        f"{'forward+backward' if w['backward'] else 'forward'}, float64 numpy, {el:.1f} s")}
     if rank == 0:
