@@ -460,9 +460,12 @@ int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, 
   a.dtype = dtype;
   a.causal = causal ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
-  // enough ranges for about three CTAs per SM, each range a whole number of CTA steps
+  // as many ranges as fill every SM's resident CTA slots in one wave (a second, partial
+  // wave would run alone at the end), each range a whole number of CTA steps
   const int smax = decode_max_splits(Nk);
-  long long want = (3LL * dev->num_sms + a.BHkv - 1) / a.BHkv;
+  int per_sm = decode_ctas_per_sm(d, dtype, a.M);
+  if (per_sm < 1) per_sm = 1;
+  long long want = (long long)per_sm * dev->num_sms / a.BHkv;
   if (want < 1) want = 1;
   if (want > smax) want = smax;
   const int kps = decode_keys_per_step(d);

@@ -31,6 +31,7 @@
 // its own (m, l, O) over the keys it visited; the CTA merges its warps at the end.
 #include <cuda_fp16.h>
 
+#include <atomic>
 #include <type_traits>
 
 #include "internal.h"
@@ -355,6 +356,23 @@ cudaError_t launch_decode_t(const DecArgs& a, cudaStream_t stream) {
                            static_cast<uint16_t*>(a.o), a.lse, a.BHkv, a.H, a.Hkv, a.Nq, a.M, a.S);
 }
 
+// Resident split-kernel CTAs per SM (registers and shared memory decide), 0 on error.
+template <int D, int DT, int MR>
+int ctas_per_sm_t() {
+  auto kern = D == 64 ? decode_split_kernel_d64<DT, MR> : decode_split_kernel_d128<DT, MR>;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kDecThreads, 0) != cudaSuccess) return 0;
+  return n;
+}
+
+template <int D, int DT>
+int ctas_per_sm_m(int M) {
+  if (M <= 1) return ctas_per_sm_t<D, DT, 1>();
+  if (M <= 2) return ctas_per_sm_t<D, DT, 2>();
+  if (M <= 4) return ctas_per_sm_t<D, DT, 4>();
+  return ctas_per_sm_t<D, DT, 8>();
+}
+
 template <int D, int DT>
 cudaError_t launch_decode_m(const DecArgs& a, cudaStream_t stream) {
   if (a.M <= 1) return launch_decode_t<D, DT, 1>(a, stream);
@@ -366,6 +384,23 @@ cudaError_t launch_decode_m(const DecArgs& a, cudaStream_t stream) {
 }  // namespace
 
 int decode_keys_per_step(int d) { return 32 * kDecWarps + 0 * d; }
+
+int decode_ctas_per_sm(int d, int dtype, int M) {
+  // one entry per (d, dtype, row bucket); the answer depends only on the compiled kernel
+  static std::atomic<int> cache[16];
+  const int bucket = M <= 1 ? 0 : M <= 2 ? 1 : M <= 4 ? 2 : 3;
+  const int key = ((d == 128 ? 2 : 0) | (dtype == 1 ? 1 : 0)) * 4 + bucket;
+  int n = cache[key].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  switch (key >> 2) {
+    case 0: n = ctas_per_sm_m<64, 0>(M); break;
+    case 1: n = ctas_per_sm_m<64, 1>(M); break;
+    case 2: n = ctas_per_sm_m<128, 0>(M); break;
+    default: n = ctas_per_sm_m<128, 1>(M); break;
+  }
+  if (n > 0) cache[key].store(n, std::memory_order_relaxed);
+  return n;
+}
 
 cudaError_t launch_decode(const DecArgs& a, cudaStream_t stream) {
   const int key = (a.d == 128 ? 2 : 0) | (a.dtype == 1 ? 1 : 0);

@@ -165,6 +165,7 @@ struct DecArgs {
 };
 constexpr int kDecodeMaxRows = 8;
 int decode_keys_per_step(int d);
+int decode_ctas_per_sm(int d, int dtype, int M);   // resident split-kernel CTAs per SM, 0 on error
 cudaError_t launch_decode(const DecArgs& a, cudaStream_t stream);
 // Backward stages: preprocess (D, lse2, zeroed accumulator), the dK/dV kernel with
 // dQ partial sums, and the dQ conversion.
