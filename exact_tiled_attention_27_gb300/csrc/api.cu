@@ -420,6 +420,7 @@ static int decode_check(int B, int H, int Hkv, int Nq, int Nk, int d, float scal
   st = check_common(B, Hkv, Nk, d, scale, dtype);
   if (st != FA_OK) return st;
   if ((long long)(H / Hkv) * Nq > kDecodeMaxRows) return FA_ERR_SHAPE;
+  if ((long long)B * Hkv > 65535) return FA_ERR_SHAPE;   // one grid row per key/value head
   return FA_OK;
 }
 

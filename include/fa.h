@@ -165,7 +165,8 @@ int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const
  * tokens against a key/value cache.  Shapes, head grouping, the bottom-right causal
  * mask and the O = 0 / lse = -inf convention are those of fa_fwd_cross; the result
  * is the same attention (within the usual rounding).  Requires (H / Hkv) * Nq <= 8
- * (FA_ERR_SHAPE otherwise; use fa_fwd_cross for more rows).
+ * (FA_ERR_SHAPE otherwise; use fa_fwd_cross for more rows) and B * Hkv <= 65535
+ * (FA_ERR_SHAPE otherwise).
  *
  * The keys of each head are cut into ranges processed by separate CTAs on the CUDA
  * cores (the pass reads K and V once and is bound by memory bandwidth); the

@@ -146,10 +146,10 @@ def test_fp8_entry_points_validate(lib):
 def test_decode_validation_and_workspace(lib):
     C = binding.STATUS_CODE
 
-    def call(H=8, Hkv=2, Nq=1, Nk=4096, d=64, ws=P, ws_bytes=None, scale=0.125):
+    def call(H=8, Hkv=2, Nq=1, Nk=4096, d=64, ws=P, ws_bytes=None, scale=0.125, B=1):
         if ws_bytes is None:
-            ws_bytes = lib.fa_decode_workspace_size(1, H, Hkv, Nq, Nk, d)
-        return lib.fa_decode(P, P, P, P, P, ws, ws_bytes, 1, H, Hkv, Nq, Nk, d, scale, 1, 0, NULL)
+            ws_bytes = lib.fa_decode_workspace_size(B, H, Hkv, Nq, Nk, d)
+        return lib.fa_decode(P, P, P, P, P, ws, ws_bytes, B, H, Hkv, Nq, Nk, d, scale, 1, 0, NULL)
 
     assert call(Hkv=3) == C["FA_ERR_SHAPE"]
     assert call(H=16, Hkv=1) == C["FA_ERR_SHAPE"]              # 16 rows per key/value head > 8
@@ -157,6 +157,8 @@ def test_decode_validation_and_workspace(lib):
     assert call(Nk=0) == C["FA_ERR_SHAPE"]
     assert call(d=96) == C["FA_ERR_UNSUPPORTED_D"]
     assert call(scale=float("nan")) == C["FA_ERR_SCALE"]
+    assert call(B=65536, H=8, Hkv=1) == C["FA_ERR_SHAPE"]     # one grid row per key/value head: <= 65535
+    assert lib.fa_decode_workspace_size(65536, 8, 1, 1, 4096, 64) == 0
     assert call(ws=NULL) == C["FA_ERR_WORKSPACE"]
     assert call(ws_bytes=1) == C["FA_ERR_WORKSPACE"]
     # ranges of >= 256 keys, at most 128: per range B*Hkv*M rows of d float32 + one lse
