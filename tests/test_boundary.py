@@ -274,3 +274,16 @@ def test_noalloc_validates_like_fa_bwd_and_checks_its_limit(lib):
         has_gpu = False
     if not has_gpu:
         assert call() == C["FA_ERR_NO_DEVICE"]
+
+
+def test_no_cpu_fallback():
+    """The product path has no CPU route: a missing library raises, and host tensors are
+    refused before any compute."""
+    torch = pytest.importorskip("torch")
+    with pytest.raises(RuntimeError, match="not found"):
+        binding.load_library(os.path.join(ROOT, "no_such_dir", "libfa_gb300.so"))
+    q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        binding.forward(q, q, q)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        binding.backward(q, q, q, q, q, torch.zeros(1, 1, 128))
