@@ -158,7 +158,17 @@ def _scores(q, k, scale, causal, row0):
     return s
 
 
-def attn_head_fwd(q, k, v, scale, causal, row_block=None, return_sp=False):
+def _row_range(n, row_range):
+    """The query rows [lo, hi) a call covers: all n rows, or the given range."""
+    if row_range is None:
+        return 0, n
+    lo, hi = int(row_range[0]), int(row_range[1])
+    if not 0 <= lo <= hi <= n:
+        raise ValueError(f"row range {row_range} outside [0, {n}]")
+    return lo, hi
+
+
+def attn_head_fwd(q, k, v, scale, causal, row_block=None, return_sp=False, row_range=None):
     """Exact attention of one head: (O, LSE) or (O, LSE, S, P).
 
     S = scale*Q K^T (masked), m_i = max_j S_ij, E = exp(S - m), l_i = sum_j E_ij,
@@ -168,36 +178,40 @@ def attn_head_fwd(q, k, v, scale, causal, row_block=None, return_sp=False):
     [FA-chapter] "地基：流式 softmax" for the max subtraction.  [FA-chapter]
     "FlashAttention——把整件事分块塞进 SRAM" and [FA-review] "方法细节": the forward
     keeps only O and the per-row statistics (m, l); LSE = m + ln l carries both.
+
+    ``row_range=(lo, hi)`` computes only query rows lo..hi-1 (each row of O and LSE
+    depends on its own row of S alone); the arrays returned then have hi - lo rows.
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
-    n = q.shape[0]
-    rb = n if row_block is None else int(row_block)
+    lo, hi = _row_range(q.shape[0], row_range)
+    n = hi - lo
+    rb = max(n, 1) if row_block is None else int(row_block)
     o = np.empty((n, v.shape[1]), dtype=np.float64)
     lse = np.empty(n, dtype=np.float64)
     s_full = p_full = None
     if return_sp:
         s_full = np.empty((n, k.shape[0]), dtype=np.float64)
         p_full = np.empty((n, k.shape[0]), dtype=np.float64)
-    for r0 in range(0, n, rb):
-        r1 = min(n, r0 + rb)
+    for r0 in range(lo, hi, rb):
+        r1 = min(hi, r0 + rb)
         s = _scores(q[r0:r1], k, scale, causal, r0)
         m = np.max(s, axis=1, keepdims=True)
         e = np.exp(s - m)
         l = np.sum(e, axis=1, keepdims=True)
         p = e / l
-        o[r0:r1] = p @ v
-        lse[r0:r1] = (m + np.log(l))[:, 0]
+        o[r0 - lo:r1 - lo] = p @ v
+        lse[r0 - lo:r1 - lo] = (m + np.log(l))[:, 0]
         if return_sp:
-            s_full[r0:r1] = s
-            p_full[r0:r1] = p
+            s_full[r0 - lo:r1 - lo] = s
+            p_full[r0 - lo:r1 - lo] = p
     if return_sp:
         return o, lse, s_full, p_full
     return o, lse
 
 
-def attn_head_bwd(q, k, v, do, scale, causal, row_block=None):
+def attn_head_bwd(q, k, v, do, scale, causal, row_block=None, row_range=None):
     """Gradients of L = sum(dO * O) for one head: (dQ, dK, dV, D).
 
     The pages say only that the backward regenerates S and P from Q, K and the saved
@@ -209,19 +223,26 @@ def attn_head_bwd(q, k, v, do, scale, causal, row_block=None):
         dS = P o (dP - D),   dQ = scale * dS K,   dK = scale * dS^T Q.
 
     P is rebuilt here from the definition (not from any stored statistic).
+
+    dK and dV are sums over the query rows i (dV_j = sum_i P_ij dO_i, dK_j = scale *
+    sum_i dS_ij Q_i).  ``row_range=(lo, hi)`` takes only rows lo..hi-1: dQ and D are
+    then those rows' (hi - lo rows), and dK, dV are those rows' contributions to the
+    two sums, so the contributions of the parts of a partition of the rows add up to
+    the whole head's dK and dV.
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
     do = np.asarray(do, dtype=np.float64)
-    n = q.shape[0]
-    rb = n if row_block is None else int(row_block)
-    dq = np.empty_like(q)
+    lo, hi = _row_range(q.shape[0], row_range)
+    n = hi - lo
+    rb = max(n, 1) if row_block is None else int(row_block)
+    dq = np.empty((n, q.shape[1]), dtype=np.float64)
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)
     dvec = np.empty(n, dtype=np.float64)
-    for r0 in range(0, n, rb):
-        r1 = min(n, r0 + rb)
+    for r0 in range(lo, hi, rb):
+        r1 = min(hi, r0 + rb)
         s = _scores(q[r0:r1], k, scale, causal, r0)
         m = np.max(s, axis=1, keepdims=True)
         e = np.exp(s - m)
@@ -231,9 +252,9 @@ def attn_head_bwd(q, k, v, do, scale, causal, row_block=None):
         dp = g @ v.T
         d_i = np.sum(p * dp, axis=1, keepdims=True)
         ds = p * (dp - d_i)
-        dq[r0:r1] = scale * (ds @ k)
+        dq[r0 - lo:r1 - lo] = scale * (ds @ k)
         dk += scale * (ds.T @ q[r0:r1])
-        dvec[r0:r1] = d_i[:, 0]
+        dvec[r0 - lo:r1 - lo] = d_i[:, 0]
     return dq, dk, dv, dvec
 
 

@@ -266,3 +266,33 @@ def test_row_subset_matches_whole_head(causal):
     np.testing.assert_allclose(lse_r, lse[rows], rtol=1e-14, atol=1e-14)
     np.testing.assert_allclose(dq_r, dq[rows], rtol=1e-12, atol=1e-13)
     np.testing.assert_allclose(d_r, dvec[rows], rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_row_ranges_partition_the_head(causal):
+    """Forward rows and backward contributions over a partition of the query rows
+    (ragged parts, an empty part, blocks that straddle the cuts) add up to the
+    whole head: O and LSE rows, dQ and D rows match, and the parts' dK and dV
+    contributions sum to the whole head's dK and dV.  A range whose causal mask
+    were taken from the range's own first row instead of its place in the
+    sequence would fail the causal case."""
+    r = np.random.Generator(np.random.PCG64(22))
+    n, d = 70, 5
+    q, k, v, do = (r.standard_normal((n, d)) for _ in range(4))
+    o, lse = A.attn_head_fwd(q, k, v, 0.6, causal)
+    dq, dk, dv, dvec = A.attn_head_bwd(q, k, v, do, 0.6, causal)
+    dk_sum, dv_sum = np.zeros_like(dk), np.zeros_like(dv)
+    for lo, hi in [(0, 13), (13, 13), (13, 50), (50, 70)]:
+        o_p, lse_p = A.attn_head_fwd(q, k, v, 0.6, causal, row_block=8, row_range=(lo, hi))
+        assert o_p.shape == (hi - lo, d) and lse_p.shape == (hi - lo,)
+        np.testing.assert_allclose(o_p, o[lo:hi], rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(lse_p, lse[lo:hi], rtol=1e-14, atol=1e-14)
+        dq_p, dk_p, dv_p, d_p = A.attn_head_bwd(q, k, v, do, 0.6, causal, row_block=8, row_range=(lo, hi))
+        np.testing.assert_allclose(dq_p, dq[lo:hi], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(d_p, dvec[lo:hi], rtol=1e-12, atol=1e-13)
+        dk_sum += dk_p
+        dv_sum += dv_p
+    np.testing.assert_allclose(dk_sum, dk, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(dv_sum, dv, rtol=1e-12, atol=1e-13)
+    with pytest.raises(ValueError):
+        A.attn_head_fwd(q, k, v, 0.6, causal, row_range=(5, 71))
