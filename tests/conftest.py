@@ -9,3 +9,10 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
     config.addinivalue_line("markers", "slow: long-running CPU test")
+
+
+def pytest_sessionfinish(session, exitstatus):
+    # stop the oracle's process pool if a test started it
+    mod = sys.modules.get("tests.oracle_jobs")
+    if mod is not None:
+        mod.shutdown()

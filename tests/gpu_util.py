@@ -2,12 +2,13 @@
 float64, the comparison metrics, and the tolerances the parity tests enforce.
 
 Tolerances (stated for the 16-bit inputs against the float64 oracle):
-  O:            max |err| <= 2e-2 * mult and ||err||_2 / ||ref||_2 <= 5e-3, where mult
-                is the factor the Gaussian inputs were multiplied by (1 for unit-scale
-                data, 3 for the "x3" sweep).  O is a convex combination of V rows, so its
-                magnitude -- and the spacing of the 16-bit grid it is rounded to --
-                grows with mult; at mult = 3 the exact O rounded to bf16 already errs by
-                up to 0.031 > 2e-2.
+  O:            |err| <= 2e-2 + ulp(O_ref)/2 element by element, and
+                ||err||_2 / ||ref||_2 <= 5e-3.  ulp(x) is the spacing of the output's
+                16-bit grid at |x| (2^(e-7) for bf16 and 2^(e-10) for fp16 when
+                2^e <= |x| < 2^(e+1)): O is returned in the 16-bit type, and even the
+                exact O rounded to nearest errs by up to half of that spacing -- 0.031
+                in bf16 at |O| in [8, 16), which the inputs scaled by 3 reach -- so the
+                stated 2e-2 bounds what the kernel adds on top of that last rounding.
   lse:          max |err| <= 1e-3
   dQ, dK, dV:   ||err||_2 / ||ref||_2 <= 1e-2
 
@@ -57,12 +58,26 @@ def rel_l2(a, ref):
     return num / den if den > 0 else num
 
 
-def check_forward(o, lse, o_ref, lse_ref, label="", mult=1.0):
+def half_ulp(x, dtype):
+    """Half the spacing of the 16-bit grid (bf16: 8 significant bits, fp16: 11) at |x|,
+    element by element; for |x| in [2^e, 2^(e+1)) that is 2^(e-8) or 2^(e-11).  fp16's
+    subnormal spacing 2^-24 is the floor."""
+    bits = 8 if dtype == "bf16" else 11
+    _, ex = np.frexp(np.abs(np.asarray(x, dtype=np.float64)))   # |x| = m 2^ex, m in [0.5, 1)
+    h = np.ldexp(1.0, ex - 1 - bits)
+    return np.maximum(h, 2.0 ** -25) if dtype == "fp16" else h
+
+
+def check_forward(o, lse, o_ref, lse_ref, label="", dtype="bf16"):
+    """O element by element within 2e-2 + half an ulp of the 16-bit output grid, O's
+    relative L2 error, and lse's absolute error (bounds in the module docstring)."""
     ma, rl, la = maxabs(o, o_ref), rel_l2(o, o_ref), maxabs(lse, lse_ref)
-    msg = f"{label} O maxabs={ma:.3e} (bound {O_MAXABS * mult:.1e}) relL2={rl:.3e} lse abs={la:.3e}"
+    excess = float(np.max(np.abs(o - o_ref) - half_ulp(o_ref, dtype))) if o.size else 0.0
+    msg = (f"{label} O maxabs={ma:.3e} (beyond half an ulp of the {dtype} grid: {excess:.3e}, bound {O_MAXABS:.0e}) "
+           f"relL2={rl:.3e} lse abs={la:.3e}")
     print(msg)
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse)), msg
-    assert ma <= O_MAXABS * mult and rl <= O_RELL2 and la <= LSE_ABS, msg
+    assert excess <= O_MAXABS and rl <= O_RELL2 and la <= LSE_ABS, msg
     return ma, rl, la
 
 

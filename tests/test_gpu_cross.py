@@ -58,7 +58,7 @@ def test_cross_matches_oracle(B, H, Hkv, Nq, Nk, d, dtype, causal):
         assert np.all(np.isneginf(lse[dead])), "rows with no visible key must have lse = -inf"
         assert np.all(o[dead] == 0.0), "rows with no visible key must have O = 0"
     live = ~dead
-    G.check_forward(o[live], lse[live], o_ref[live], lse_ref[live], f"cross B{B} H{H}/{Hkv} {Nq}x{Nk} d{d}")
+    G.check_forward(o[live], lse[live], o_ref[live], lse_ref[live], f"cross B{B} H{H}/{Hkv} {Nq}x{Nk} d{d}", dtype)
 
 
 @pytest.mark.parametrize("causal", [True, False])

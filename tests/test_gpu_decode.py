@@ -50,7 +50,7 @@ def test_decode_matches_oracle(B, H, Hkv, Nq, Nk, d, dtype, causal):
     if dead.any():
         assert np.all(np.isneginf(lse[dead])) and np.all(o[dead] == 0.0)
     live = ~dead
-    G.check_forward(o[live], lse[live], o_ref[live], lse_ref[live], f"decode B{B} H{H}/{Hkv} {Nq}x{Nk} d{d}")
+    G.check_forward(o[live], lse[live], o_ref[live], lse_ref[live], f"decode B{B} H{H}/{Hkv} {Nq}x{Nk} d{d}", dtype)
 
 
 def test_decode_agrees_with_tile_forward_and_is_repeatable():

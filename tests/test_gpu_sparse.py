@@ -47,7 +47,7 @@ def test_butterfly_matches_oracle(B, H, N, d, dtype, causal):
         for h in range(H):
             f = lambda name: bits_to_f64(getattr(c, name)[b, h], dtype)  # noqa: E731
             o_ref, lse_ref = oracle.attn_masked_head_fwd(f("q"), f("k"), f("v"), c.scale, mask)
-            G.check_forward(G.to_f64(o[b, h]), G.to_f64(lse[b, h]), o_ref, lse_ref, f"butterfly N{N} ({b},{h})")
+            G.check_forward(G.to_f64(o[b, h]), G.to_f64(lse[b, h]), o_ref, lse_ref, f"butterfly N{N} ({b},{h})", dtype)
             refs = oracle.attn_masked_head_bwd(f("q"), f("k"), f("v"), f("do"), c.scale, mask)
             G.check_backward([G.to_f64(x[b, h]) for x in (dq, dk, dv)], refs, f"butterfly N{N} ({b},{h})")
 
