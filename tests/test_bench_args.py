@@ -16,3 +16,19 @@ def test_oracle_threads_defaults_to_every_core(monkeypatch):
     assert bench.oracle_threads() == os.cpu_count()
     monkeypatch.setattr(bench, "CPU_THREADS", "3")
     assert bench.oracle_threads() == 3
+
+
+def test_visible_pairs_of_row_ranges_add_up():
+    for N in (1, 7, 128, 1000):
+        for causal in (False, True):
+            cuts = sorted({0, N, N // 3, N // 2})
+            total = sum(bench.visible_pairs(N, causal, lo, hi) for lo, hi in zip(cuts, cuts[1:]))
+            assert total == (N * (N + 1) // 2 if causal else N * N)
+    assert bench.visible_pairs(10, True, 0, 1) == 1 and bench.visible_pairs(10, True, 9, 10) == 10
+
+
+def test_oracle_sample_is_bounded_and_counts_work():
+    w = bench.WORKLOADS["c1_tiny"]
+    n, rows, el, tf = bench.oracle_sample(w, 0.0, max_samples=2)
+    assert n == 1 and rows == w["N"] and el > 0 and tf > 0
+    assert "whole (b,h) heads" in bench.sample_text(w, n, rows, el)
