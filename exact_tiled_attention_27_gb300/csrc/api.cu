@@ -26,11 +26,31 @@ struct DeviceInfo {
   long long l2_bytes = 0;
   int major = 0;
   unsigned int* err_word = nullptr;
+  unsigned long long ctx = 0;   // context the error word's address was looked up in
 };
 
 std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Driver calls that identify the current context (resolved once through the runtime's
+// entry-point query, so the library needs no link against the driver library).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+CtxGetCurrentFn g_ctx_current = nullptr;
+CtxGetIdFn g_ctx_id = nullptr;
+std::once_flag g_ctx_once;
+
+void* driver_fn(const char* name, int version) {
+  cudaDriverEntryPointQueryResult q;
+  void* fn = nullptr;
+  if (cudaGetDriverEntryPointByVersion(name, &fn, version, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return fn;
+}
 
 int get_device(DeviceInfo** out) {
   int dev = -1;
@@ -47,11 +67,6 @@ int get_device(DeviceInfo** out) {
       return FA_ERR_NO_DEVICE;
     }
     if (prop.major != 10) return FA_ERR_NO_DEVICE;   // tcgen05 / TMEM need the sm_100 family
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) {
-      cudaGetLastError();
-      return FA_ERR_NO_DEVICE;
-    }
     if (g_encode == nullptr) {
       cudaDriverEntryPointQueryResult q;
       void* fn = nullptr;
@@ -66,8 +81,19 @@ int get_device(DeviceInfo** out) {
     d.num_sms = prop.multiProcessorCount;
     d.l2_bytes = prop.l2CacheSize;
     d.major = prop.major;
-    d.err_word = static_cast<unsigned int*>(p);
     d.ready = true;
+  }
+  // The error word's device address belongs to the context it was looked up in; a
+  // device reset (or a context the caller made current) gets a new one.
+  const unsigned long long ctx = current_context_id();
+  if (d.err_word == nullptr || ctx == 0 || ctx != d.ctx) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return FA_ERR_NO_DEVICE;
+    }
+    d.err_word = static_cast<unsigned int*>(p);
+    d.ctx = current_context_id();   // the lookup creates the context if there was none
   }
   *out = &d;
   return FA_OK;
@@ -177,6 +203,19 @@ __global__ void debug_wait_kernel(unsigned int* err_word, uint64_t limit_ns) {
 }
 
 }  // namespace
+
+unsigned long long current_context_id() {
+  std::call_once(g_ctx_once, [] {
+    g_ctx_current = reinterpret_cast<CtxGetCurrentFn>(driver_fn("cuCtxGetCurrent", 4000));
+    g_ctx_id = reinterpret_cast<CtxGetIdFn>(driver_fn("cuCtxGetId", 12000));
+  });
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (g_ctx_current == nullptr || g_ctx_id == nullptr || g_ctx_current(&c) != CUDA_SUCCESS || c == nullptr ||
+      g_ctx_id(c, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
 
 cudaError_t launch_debug_wait(unsigned int* err_word, uint64_t limit_ns, cudaStream_t stream) {
   debug_wait_kernel<<<1, 32, 0, stream>>>(err_word, limit_ns);
@@ -493,7 +532,7 @@ const char* fa_strerror(int status) {
   switch (status) {
     case FA_OK: return "ok";
     case FA_ERR_NULL: return "a required pointer is NULL";
-    case FA_ERR_SHAPE: return "B, H and N must be >= 1 and B*H*N < 2^31";
+    case FA_ERR_SHAPE: return "B, H and N must be >= 1, B*H <= 2^30 and B*H*N < 2^31";
     case FA_ERR_UNSUPPORTED_D: return "head_dim must be 64 or 128";
     case FA_ERR_DTYPE: return "dtype must be FA_BF16 or FA_FP16";
     case FA_ERR_ALIGN: return "tensor base addresses must be 16-byte aligned (lse: 4-byte)";

@@ -149,6 +149,11 @@ cudaError_t launch_overlapped(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 
+// Unique id of the calling thread's current CUDA context (0 when there is none or it
+// cannot be read).  Device addresses of the library's __device__ variables are valid
+// in the context they were looked up in; a device reset replaces the context.
+unsigned long long current_context_id();
+
 // Split-key decode: the M = (H/Hkv)*Nq query rows of each key/value head (M <= 8)
 // against Nk keys cut into S ranges of `chunk` keys; partial results in opart/lpart
 // when S > 1.

@@ -11,12 +11,13 @@
 //
 // The array (kScratchBytes) is a file-scope __device__ variable, so every GPU on which
 // the library's kernels are loaded holds it until the process exits.  Its device
-// address is looked up once per device, on the first call made on that device, with
-// that device current; that first call should therefore come before any stream
-// capture.  All calls on a device share the one array and it keeps the last call's
-// contents: the preprocess launch rewrites the statistics and zeroes the accumulator
-// every call, and two calls whose work overlaps on the GPU (different streams, or
-// different host threads) race on it.
+// address is looked up on the first call made on that device, with that device
+// current, and again whenever the current context of the device has changed since (a
+// device reset replaces the context, and with it the array's address); that first
+// call should therefore come before any stream capture.  All calls on a device share
+// the one array and it keeps the last call's contents: the preprocess launch rewrites
+// the statistics and zeroes the accumulator every call, and two calls whose work
+// overlaps on the GPU (different streams, or different host threads) race on it.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -34,8 +35,10 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};   // context each address was looked up in
 
-// Device address of the scratch array on the current device (looked up once per device).
+// Device address of the scratch array on the current device, looked up on the first
+// call in each context of the device.
 int scratch_for_current_device(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -43,7 +46,8 @@ int scratch_for_current_device(void** out) {
     return FA_ERR_NO_DEVICE;
   }
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
+  const unsigned long long ctx = current_context_id();
+  if (g_scratch_ptr[dev] == nullptr || ctx == 0 || ctx != g_scratch_ctx[dev]) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || p == nullptr) {
@@ -51,6 +55,7 @@ int scratch_for_current_device(void** out) {
       return FA_ERR_NO_DEVICE;
     }
     g_scratch_ptr[dev] = p;
+    g_scratch_ctx[dev] = current_context_id();
   }
   *out = g_scratch_ptr[dev];
   return FA_OK;

@@ -29,8 +29,10 @@
  *    is the row maximum of scale*q.k and l = sum_j exp(scale*q.k_j - m).  It carries
  *    the pair (m, l) that the pages' forward keeps for the backward.
  *  - Causal masking: key j is visible to query i iff j <= i (lower triangle).
- *  - Supported: d in {64, 128}; N >= 1; B >= 1; H >= 1; B*H*N < 2^31;
- *    scale finite and > 0; dtype FA_BF16 or FA_FP16.
+ *  - Supported: d in {64, 128}; N >= 1; B >= 1; H >= 1; B*H <= 2^30 and
+ *    B*H*N < 2^31 rows per tensor (so row indices fit in 32 bits); scale finite and
+ *    > 0; dtype FA_BF16 or FA_FP16.  The row limit never binds a call whose tensors
+ *    fit in one GPU: 2^31 rows of q and of o alone take 512 GiB at d = 64.
  *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the legacy
  *    default stream) and runs on the calling thread's current CUDA device.
  *  - Ownership: the caller owns every buffer.  fa_fwd and fa_bwd allocate no
@@ -288,7 +290,9 @@ int fa_bwd_dq_convert(const void* q, const void* k, const void* v, const void* o
  *     about 8.1 million elements of B*H*N*d).
  *   - No cudaMalloc, cudaFree or other allocating call is made.
  *   - The first call on each device looks up the array's device address (with that
- *     device current); make that first call before any stream capture.
+ *     device current); make that first call before any stream capture.  The lookup
+ *     is repeated when the device's current context has changed since (a device
+ *     reset replaces the context and the address).
  *   - Every call on a device shares the one array and it keeps the last call's
  *     contents (each call re-zeroes what must start at zero).  Calls whose work
  *     overlaps on the GPU -- two streams, or two host threads -- race on it.

@@ -83,6 +83,20 @@ def test_forward_validation_codes(lib):
     assert fwd(lib, o=PM) == C["FA_ERR_ALIGN"]
 
 
+def test_size_limits_are_pinned(lib):
+    """The size limits: B*H <= 2^30 heads and B*H*N < 2^31 rows per tensor.  A call at
+    the limit passes the shape check (it then stops at the null pointer, before any
+    device work); one row more is FA_ERR_SHAPE.  Any call that fits in device memory
+    is inside these limits: 2^31 rows of Q and of O alone take 512 GiB at d = 64."""
+    C = binding.STATUS_CODE
+    for B, H, N in [(1, 2, (1 << 30) - 1), (1 << 10, 1 << 10, (1 << 11) - 1), (1, 1 << 30, 1)]:
+        assert fwd(lib, q=NULL, B=B, H=H, N=N) == C["FA_ERR_NULL"]
+        assert bwd(lib, q=NULL, ws=P, ws_bytes=1 << 62, B=B, H=H, N=N) == C["FA_ERR_NULL"]
+    for B, H, N in [(1, 2, 1 << 30), (1 << 10, 1 << 10, 1 << 11), (1, (1 << 30) + 1, 1), (2, 1 << 30, 1)]:
+        assert fwd(lib, q=NULL, B=B, H=H, N=N) == C["FA_ERR_SHAPE"]
+        assert lib.fa_bwd_workspace_size(B, H, N, 64) == 0
+
+
 def fwd_cross(lib, q=P, k=P, B=1, H=4, Hkv=2, Nq=3, Nk=300, d=64, scale=0.125, causal=1, dtype=0):
     return lib.fa_fwd_cross(q, k, P, P, P, B, H, Hkv, Nq, Nk, d, scale, causal, dtype, NULL)
 
