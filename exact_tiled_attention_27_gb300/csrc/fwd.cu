@@ -89,7 +89,8 @@ struct FwdCfg {
   static constexpr int kVFull = kKFull + kStages;           // [kStages]
   static constexpr int kKVEmpty = kVFull + kStages;         // [kStages]
   static constexpr int kSFull = kKVEmpty + kStages;         // [2]
-  static constexpr int kPFull = kSFull + 2;                 // [2]
+  static constexpr int kPHalf = kSFull + 2;                 // [2] first 64 keys of P written
+  static constexpr int kPFull = kPHalf + 2;                 // [2]
   static constexpr int kOFull = kPFull + 2;                 // [2]
   static constexpr int kOEmpty = kOFull + 2;                // [2]
   static constexpr int kDrain = kOEmpty + 2;
@@ -140,6 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(C::kSFull + t), 1);
+      mbar_init(bar(C::kPHalf + t), kTileRows);
       mbar_init(bar(C::kPFull + t), kTileRows);
       mbar_init(bar(C::kOFull + t), 1);
       mbar_init(bar(C::kOEmpty + t), kTileRows);
@@ -308,24 +310,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t vbase = smem_u32(smem + C::kOffV + st * C::kTileBytes);
           const uint32_t knext = smem_u32(smem + C::kOffK + stn * C::kTileBytes);
+          // V's second 64-column block is the next 16 KB (d = 128) or the block of ones
+          const uint32_t lbo = C::kOnesCol ? smem_u32(smem + C::kOffOnes) - vbase : kChunkBytes;
+          const uint64_t vd = sdesc_sw128(vbase, lbo, 1024);
+          // O_t += P_t V for keys [16*kk0, 16*kk1) of the block: B = V (keys x d), d
+          // contiguous: MN-major; 16 keys = 16 rows of 128 bytes
+          auto issue_pv = [&](int t, int kk0, int kk1) {
+#pragma unroll
+            for (int kk = kk0; kk < kk1; ++kk)
+              umma_ts(tmem + C::tm_o(t), tmem + C::tm_p(t) + kk * 8, vd + ((kk * 16 * 128) >> 4), idesc_pv,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+          };
           for (int t = 0; t < 2; ++t) {
             if (j >= n[t]) continue;
-            if (!wait_warp(bar(C::kPFull + t), c[t] & 1, ctl, 0x205) ||
+            // the first 64 keys' P are in tensor memory: their product overlaps the
+            // softmax's exponentials of the other 64
+            if (!wait_warp(bar(C::kPHalf + t), c[t] & 1, ctl, 0x205) ||
                 (j == 0 && e[t] > 0 && !wait_warp(bar(C::kOEmpty + t), (e[t] - 1) & 1, ctl, 0x206))) {
               ok = false;
               break;
             }
             tc_fence_after();
+            if (elect_one()) issue_pv(t, 0, kTileRows / 32);
+            __syncwarp();
+            if (!wait_warp(bar(C::kPFull + t), c[t] & 1, ctl, 0x207)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
             if (elect_one()) {
-              // V's second 64-column block is the next 16 KB (d = 128) or the block of ones
-              const uint32_t lbo = C::kOnesCol ? smem_u32(smem + C::kOffOnes) - vbase : kChunkBytes;
-              const uint64_t vd = sdesc_sw128(vbase, lbo, 1024);
-#pragma unroll
-              for (int kk = 0; kk < kTileRows / 16; ++kk) {
-                // B = V (keys x d), d contiguous: MN-major; 16 keys = 16 rows of 128 bytes
-                umma_ts(tmem + C::tm_o(t), tmem + C::tm_p(t) + kk * 8, vd + ((kk * 16 * 128) >> 4), idesc_pv,
-                        (j > 0 || kk > 0) ? 1u : 0u);
-              }
+              issue_pv(t, kTileRows / 32, kTileRows / 16);
               if (j + 1 < n[t]) {
                 issue_s(t, qbase0 + t * C::kTileBytes, knext);
                 umma_commit(bar(C::kSFull + t));
@@ -422,23 +436,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float alpha = (GEN && m_new == m) ? 1.0f : ex2_approx(m - m_new);
         const float nm = (GEN && m_new == -INFINITY) ? 0.0f : -m_new;
         const uint64_t nm2 = f2_pack(nm, nm);
-        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};    // sum of P as computed (for lse)
-        uint64_t accr[4] = {0ull, 0ull, 0ull, 0ull};   // d = 128: sum of P as rounded for the MMA
-        uint32_t pk[64];
-#pragma unroll
-        for (int q = 0; q < 64; ++q) {
-          float x0, x1;
-          f2_unpack(ffma2(f2_pack(s[2 * q], s[2 * q + 1]), c2, nm2), x0, x1);
-          const float p0 = ex2_approx(x0);
-          const float p1 = ex2_approx(x1);
-          acc[q & 3] = fadd2(acc[q & 3], f2_pack(p0, p1));
-          pk[q] = pack2<DT>(p0, p1);
-          if constexpr (!C::kOnesCol) accr[q & 3] = fadd2(accr[q & 3], unpack2_f2<DT>(pk[q]));
-        }
-        tmem_st32(p_addr, pk);
-        tmem_st32(p_addr + 32, pk + 32);
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
-          // O holds every earlier P.V (committed before this S); bring it to the new maximum
+          // O holds every earlier P.V (committed before this S); bring it to the new
+          // maximum before this block's first P.V adds to it
 #pragma unroll
           for (int q = 0; q < D / 32; ++q) {
             uint32_t orr[32];
@@ -459,6 +459,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st16(o_addr + D, orr);
           }
         }
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};    // sum of P as computed (for lse)
+        uint64_t accr[4] = {0ull, 0ull, 0ull, 0ull};   // d = 128: sum of P as rounded for the MMA
+        // P in two halves of 64 keys; each half is handed to the MMA warp as soon as it
+        // is in tensor memory
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int q = 0; q < 32; ++q) {
+            const int qq = hf * 32 + q;
+            float x0, x1;
+            f2_unpack(ffma2(f2_pack(s[2 * qq], s[2 * qq + 1]), c2, nm2), x0, x1);
+            const float p0 = ex2_approx(x0);
+            const float p1 = ex2_approx(x1);
+            acc[q & 3] = fadd2(acc[q & 3], f2_pack(p0, p1));
+            pk[q] = pack2<DT>(p0, p1);
+            if constexpr (!C::kOnesCol) accr[q & 3] = fadd2(accr[q & 3], unpack2_f2<DT>(pk[q]));
+          }
+          tmem_st32(p_addr + hf * 32, pk);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(bar(hf == 0 ? C::kPHalf + t : C::kPFull + t));
+        }
         float a0, a1, b0, b1;
         f2_unpack(fadd2(acc[0], acc[1]), a0, a1);
         f2_unpack(fadd2(acc[2], acc[3]), b0, b1);
@@ -470,9 +493,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           lr = lr * alpha + ((a0 + a1) + (b0 + b1));
         }
         m = m_new;
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(bar(C::kPFull + t));
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue

@@ -65,7 +65,8 @@ struct F8Cfg {
   static constexpr int kVFull = kKFull + kStages;
   static constexpr int kKVEmpty = kVFull + kStages;
   static constexpr int kSFull = kKVEmpty + kStages;         // [2]
-  static constexpr int kPFull = kSFull + 2;                 // [2]
+  static constexpr int kPHalf = kSFull + 2;                 // [2] codes of the first 64 keys written
+  static constexpr int kPFull = kPHalf + 2;                 // [2]
   static constexpr int kOFull = kPFull + 2;                 // [2]
   static constexpr int kOEmpty = kOFull + 2;                // [2]
   static constexpr int kDrain = kOEmpty + 2;
@@ -112,6 +113,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(C::kSFull + t), 1);
+      mbar_init(bar(C::kPHalf + t), kTileRows);
       mbar_init(bar(C::kPFull + t), kTileRows);
       mbar_init(bar(C::kOFull + t), 1);
       mbar_init(bar(C::kOEmpty + t), kTileRows);
@@ -244,20 +246,33 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         }
         const uint32_t vbase = smem_u32(smem + C::kOffV + st * C::kTileBytes);
         const uint32_t knext = smem_u32(smem + C::kOffK + stn * C::kTileBytes);
+        // O += P V for keys [32*kk0, 32*kk1): A = P from tensor memory (32 keys = 8
+        // columns), B = V^T (d x keys)
+        auto issue_pv = [&](int t, int kk0, int kk1) {
+#pragma unroll
+          for (int kk = kk0; kk < kk1; ++kk)
+            umma_ts_f8(tmem + C::tm_o(t), tmem + C::tm_s(t) + kk * 8, sdesc_sw128(vbase + kk * 32, 16, 1024),
+                       idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+        };
         for (int t = 0; t < 2; ++t) {
           if (j >= n[t]) continue;
-          if (!wait_warp(bar(C::kPFull + t), c[t] & 1, ctl, 0xa05) ||
+          // the first 64 keys' codes are in tensor memory: their product overlaps the
+          // softmax's exponentials of the other 64
+          if (!wait_warp(bar(C::kPHalf + t), c[t] & 1, ctl, 0xa05) ||
               (j == 0 && e[t] > 0 && !wait_warp(bar(C::kOEmpty + t), (e[t] - 1) & 1, ctl, 0xa06))) {
             ok = false;
             break;
           }
           tc_fence_after();
+          if (elect_one()) issue_pv(t, 0, kTileRows / 64);
+          __syncwarp();
+          if (!wait_warp(bar(C::kPFull + t), c[t] & 1, ctl, 0xa07)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
           if (elect_one()) {
-#pragma unroll
-            for (int kk = 0; kk < kTileRows / 32; ++kk)   // O += P V: A = P from tensor memory (32 keys = 8
-                                                          // columns), B = V^T (d x keys)
-              umma_ts_f8(tmem + C::tm_o(t), tmem + C::tm_s(t) + kk * 8, sdesc_sw128(vbase + kk * 32, 16, 1024),
-                         idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+            issue_pv(t, kTileRows / 64, kTileRows / 32);
             if (j + 1 < n[t]) {
               issue_s(t, qbase0 + t * C::kTileBytes, knext);
               umma_commit(bar(C::kSFull + t));
@@ -345,21 +360,9 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         const uint64_t c2 = f2_pack(cj, cj);
         const float off = vj + kPHeadroom - m_new;
         const uint64_t off2 = f2_pack(off, off);
-        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-        uint32_t pk[32];
-#pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          float x0, x1, x2, x3;
-          f2_unpack(ffma2(f2_pack(s[4 * q], s[4 * q + 1]), c2, off2), x0, x1);
-          f2_unpack(ffma2(f2_pack(s[4 * q + 2], s[4 * q + 3]), c2, off2), x2, x3);
-          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
-          acc[q & 3] = fadd2(acc[q & 3], fadd2(f2_pack(p0, p1), f2_pack(p2, p3)));
-          pk[q] = pack4_e4m3(p0, p1, p2, p3);
-        }
-        // P (four E4M3 codes per column) over the first 32 columns of S_t
-        tmem_st32(s_addr, pk);
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
-          // O holds every earlier P.V (committed before this S): bring it to the new maximum
+          // O holds every earlier P.V (committed before this S): bring it to the new
+          // maximum before this block's first P.V adds to it
 #pragma unroll
           for (int q = 0; q < D / 32; ++q) {
             uint32_t orr[32];
@@ -370,7 +373,27 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
             tmem_st32(o_addr + q * 32, orr);
           }
+        }
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+        // P (four E4M3 codes per column) over the first 32 columns of S_t, in two halves of
+        // 64 keys, each handed to the MMA warp as soon as it is in tensor memory
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const int qq = hf * 16 + q;
+            float x0, x1, x2, x3;
+            f2_unpack(ffma2(f2_pack(s[4 * qq], s[4 * qq + 1]), c2, off2), x0, x1);
+            f2_unpack(ffma2(f2_pack(s[4 * qq + 2], s[4 * qq + 3]), c2, off2), x2, x3);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+            acc[q & 3] = fadd2(acc[q & 3], fadd2(f2_pack(p0, p1), f2_pack(p2, p3)));
+            pk[q] = pack4_e4m3(p0, p1, p2, p3);
+          }
+          tmem_st16(s_addr + hf * 16, pk);
           tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(bar(hf == 0 ? C::kPHalf + t : C::kPFull + t));
         }
         float a0, a1, b0, b1;
         f2_unpack(fadd2(acc[0], acc[1]), a0, a1);
@@ -381,9 +404,6 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         l = l * alpha + rowsum * inv_sv;
         lr = lr * alpha + (rowsum + (round_e4m3(pmax) - pmax)) * inv_sv;
         m = m_new;
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(bar(C::kPFull + t));
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
