@@ -2,13 +2,24 @@
 float64, the comparison metrics, and the tolerances the parity tests enforce.
 
 Tolerances (stated for the 16-bit inputs against the float64 oracle):
-  O:            |err| <= 2e-2 + ulp(O_ref)/2 element by element, and
-                ||err||_2 / ||ref||_2 <= 5e-3.  ulp(x) is the spacing of the output's
-                16-bit grid at |x| (2^(e-7) for bf16 and 2^(e-10) for fp16 when
-                2^e <= |x| < 2^(e+1)): O is returned in the 16-bit type, and even the
-                exact O rounded to nearest errs by up to half of that spacing -- 0.031
-                in bf16 at |O| in [8, 16), which the inputs scaled by 3 reach -- so the
-                stated 2e-2 bounds what the kernel adds on top of that last rounding.
+  O:            element by element |err| <= max(2e-2, r) + ulp(O_ref)/2, and
+                ||err||_2 / ||ref||_2 <= 5e-3, where
+                * ulp(x) is the spacing of the output's 16-bit grid at |x| (2^(e-7) for
+                  bf16 and 2^(e-10) for fp16 when 2^e <= |x| < 2^(e+1)): O is returned in
+                  the 16-bit type, and even the exact O rounded to nearest errs by up to
+                  half of that spacing (0.031 in bf16 at |O| in [8, 16), which the inputs
+                  scaled by 3 reach);
+                * r is the most that rounding the probabilities to the 16-bit type before
+                  the P.V product can move O (production kernels multiply 16-bit tiles):
+                  with p_j -> p_j (1 + d_j), |d_j| <= u (unit roundoff, 2^-8 for bf16,
+                  2^-11 for fp16) and O divided by the sum of the rounded p, O_i moves by
+                  sum_j w_ij (d_j - dbar)(V_j - O_i) / (1 + dbar), at most
+                  r_ic = 2u/(1-u) * sum_j P_ij |V_jc - O_ic| <= 2u/(1-u) ((P|V|)_ic + |O_ic|).
+                  The right-hand side is what the tests use (P|V| is the oracle run with
+                  |V| as the values).  For unit-scale inputs r stays below 2e-2, so the
+                  stated bound holds as stated; with inputs scaled by 3 a row whose weight
+                  is spread over keys with large |V| can reach r > 2e-2.
+                When P|V| is not supplied, r is taken as 0 (the stated 2e-2).
   lse:          max |err| <= 1e-3
   dQ, dK, dV:   ||err||_2 / ||ref||_2 <= 1e-2
 
@@ -68,16 +79,31 @@ def half_ulp(x, dtype):
     return np.maximum(h, 2.0 ** -25) if dtype == "fp16" else h
 
 
-def check_forward(o, lse, o_ref, lse_ref, label="", dtype="bf16"):
-    """O element by element within 2e-2 + half an ulp of the 16-bit output grid, O's
-    relative L2 error, and lse's absolute error (bounds in the module docstring)."""
+def unit_roundoff(dtype):
+    return 2.0 ** -8 if dtype == "bf16" else 2.0 ** -11
+
+
+def p_rounding_bound(o_ref, pv_abs, dtype):
+    """Most that rounding P to the 16-bit type can move each element of O:
+    2u/(1-u) ((P|V|) + |O|) (module docstring)."""
+    u = unit_roundoff(dtype)
+    return 2.0 * u / (1.0 - u) * (np.asarray(pv_abs) + np.abs(o_ref))
+
+
+def check_forward(o, lse, o_ref, lse_ref, label="", dtype="bf16", pv_abs=None):
+    """O element by element within max(2e-2, r) + half an ulp of the 16-bit output
+    grid, O's relative L2 error, and lse's absolute error (bounds in the module
+    docstring).  `pv_abs` = P|V| from the oracle enables the P-rounding term r."""
     ma, rl, la = maxabs(o, o_ref), rel_l2(o, o_ref), maxabs(lse, lse_ref)
+    allow = O_MAXABS if pv_abs is None else np.maximum(O_MAXABS, p_rounding_bound(o_ref, pv_abs, dtype))
+    over = np.abs(o - o_ref) - half_ulp(o_ref, dtype) - allow
+    worst = float(np.max(over)) if o.size else -1.0
     excess = float(np.max(np.abs(o - o_ref) - half_ulp(o_ref, dtype))) if o.size else 0.0
-    msg = (f"{label} O maxabs={ma:.3e} (beyond half an ulp of the {dtype} grid: {excess:.3e}, bound {O_MAXABS:.0e}) "
-           f"relL2={rl:.3e} lse abs={la:.3e}")
+    msg = (f"{label} O maxabs={ma:.3e} (beyond half an ulp of the {dtype} grid: {excess:.3e}; "
+           f"margin to the bound {-worst:.3e}) relL2={rl:.3e} lse abs={la:.3e}")
     print(msg)
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse)), msg
-    assert excess <= O_MAXABS and rl <= O_RELL2 and la <= LSE_ABS, msg
+    assert worst <= 0.0 and rl <= O_RELL2 and la <= LSE_ABS, msg
     return ma, rl, la
 
 

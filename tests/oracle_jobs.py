@@ -46,11 +46,17 @@ def shutdown():
 
 
 def head_fwd(q_bits, k_bits, v_bits, dtype, scale, causal, row_block, row_range):
-    """(O, LSE) of query rows row_range of one head, from its 16-bit inputs."""
+    """(O, LSE, P|V|) of query rows row_range of one head, from its 16-bit inputs;
+    P|V| (the oracle run with |V| as the values) sizes the P-rounding term of the O
+    tolerance."""
+    import numpy as np
+
     import oracle
     from exact_tiled_attention_27_gb300.inputs import bits_to_f64
     q, k, v = (bits_to_f64(x, dtype) for x in (q_bits, k_bits, v_bits))
-    return oracle.attn_head_fwd(q, k, v, scale, causal, row_block, row_range=row_range)
+    o, lse = oracle.attn_head_fwd(q, k, v, scale, causal, row_block, row_range=row_range)
+    pv_abs, _ = oracle.attn_head_fwd(q, k, np.abs(v), scale, causal, row_block, row_range=row_range)
+    return o, lse, pv_abs
 
 
 def head_bwd(q_bits, k_bits, v_bits, do_bits, dtype, scale, causal, row_block, row_range):
@@ -82,9 +88,10 @@ class HeadJobs:
         self.bwd = [ex.submit(head_bwd, q, k, v, do, *args, r) for r in self.ranges] if with_bwd else None
 
     def forward(self):
+        """(O, LSE, P|V|) of the whole head."""
         import numpy as np
         parts = [f.result() for f in self.fwd]
-        return np.concatenate([p[0] for p in parts]), np.concatenate([p[1] for p in parts])
+        return tuple(np.concatenate([p[i] for p in parts]) for i in range(3))
 
     def backward(self):
         import numpy as np

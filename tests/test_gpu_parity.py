@@ -35,7 +35,8 @@ def run_and_check(case, with_bwd=True, label=""):
     torch.cuda.synchronize()
     q64, k64, v64 = case.f64("q"), case.f64("k"), case.f64("v")
     o_ref, lse_ref = oracle.attn_fwd_ref(q64, k64, v64, case.scale, case.causal)
-    G.check_forward(G.to_f64(o), G.to_f64(lse), o_ref, lse_ref, label, case.dtype)
+    pv_abs, _ = oracle.attn_fwd_ref(q64, k64, np.abs(v64), case.scale, case.causal)
+    G.check_forward(G.to_f64(o), G.to_f64(lse), o_ref, lse_ref, label, case.dtype, pv_abs)
     if not with_bwd:
         return
     do = G.to_device(case.do, case.dtype)

@@ -67,8 +67,9 @@ def _check_heads_inline(case, o, lse, grads, heads, label):
     for b, h in heads:
         q64, k64, v64 = _f64(case, "q", b, h), _f64(case, "k", b, h), _f64(case, "v", b, h)
         o_ref, lse_ref = oracle.attn_head_fwd(q64, k64, v64, case.scale, case.causal)
+        pv_abs, _ = oracle.attn_head_fwd(q64, k64, np.abs(v64), case.scale, case.causal)
         G.check_forward(G.to_f64(o[b, h]), G.to_f64(lse[b, h]), o_ref, lse_ref, f"{label} head ({b},{h})",
-                        case.dtype)
+                        case.dtype, pv_abs)
         if grads is not None:
             refs = oracle.attn_head_bwd(q64, k64, v64, _f64(case, "do", b, h), case.scale, case.causal)
             G.check_backward([G.to_f64(g[b, h]) for g in grads], refs[:3], f"{label} head ({b},{h})")
@@ -118,8 +119,8 @@ class PooledRun:
         for bh in self.heads:
             label = f"{self.name} head {bh}"
             o, lse, g = self.gpu[bh]
-            o_ref, lse_ref = self.jobs[bh].forward()
-            G.check_forward(o.astype(np.float64), lse.astype(np.float64), o_ref, lse_ref, label, self.dtype)
+            o_ref, lse_ref, pv_abs = self.jobs[bh].forward()
+            G.check_forward(o.astype(np.float64), lse.astype(np.float64), o_ref, lse_ref, label, self.dtype, pv_abs)
             if g is not None:
                 G.check_backward([x.astype(np.float64) for x in g], self.jobs[bh].backward(), label)
         if self.ident is not None:

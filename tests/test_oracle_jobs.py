@@ -22,12 +22,15 @@ def test_row_ranges_cover_rows_once():
 def test_pooled_head_equals_whole_head(causal):
     case = make_case(2, 2, 300, 64, "bf16", causal, workload_index=95, mult=3.0)
     jobs = oracle_jobs.HeadJobs(case, 1, 0, parts=3, row_block=64, with_bwd=True)
-    o, lse = jobs.forward()
+    o, lse, pv_abs = jobs.forward()
     dq, dk, dv = jobs.backward()
     f = lambda n: case.f64(n)[1, 0]  # noqa: E731
     o_ref, lse_ref = oracle.attn_head_fwd(f("q"), f("k"), f("v"), case.scale, causal)
     dq_ref, dk_ref, dv_ref, _ = oracle.attn_head_bwd(f("q"), f("k"), f("v"), f("do"), case.scale, causal)
     np.testing.assert_allclose(o, o_ref, rtol=1e-13, atol=1e-13)
     np.testing.assert_allclose(lse, lse_ref, rtol=1e-13, atol=1e-13)
+    pv_ref, _ = oracle.attn_head_fwd(f("q"), f("k"), np.abs(f("v")), case.scale, causal)
+    np.testing.assert_allclose(pv_abs, pv_ref, rtol=1e-13, atol=1e-13)
+    assert np.all(pv_abs >= np.abs(o) - 1e-12)   # |P V| <= P |V|
     for a, b in [(dq, dq_ref), (dk, dk_ref), (dv, dv_ref)]:
         np.testing.assert_allclose(a, b, rtol=1e-11, atol=1e-12)
