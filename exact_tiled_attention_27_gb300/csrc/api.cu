@@ -171,18 +171,17 @@ constexpr size_t kAlign = 256;
 size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct WsLayout {
-  size_t sched_off, dvec_off, lse2_off, acc_off, total;
+  size_t sched_off, stats_off, acc_off, total;
   int Npad;
 };
 
 WsLayout ws_layout(int B, int H, int N, int d) {
   WsLayout w;
   w.Npad = (N + 127) / 128 * 128;
-  const size_t rows = (size_t)B * H * w.Npad;
+  const size_t blocks = (size_t)B * H * (w.Npad / 128);
   w.sched_off = 0;                        // tile counter of the dK/dV kernel
-  w.dvec_off = kAlign;
-  w.lse2_off = w.dvec_off + round_up(rows * 4);
-  w.acc_off = w.lse2_off + round_up(rows * 4);
+  w.stats_off = kAlign;                   // per-query-block statistics tiles
+  w.acc_off = w.stats_off + round_up(blocks * kStatsTileBytes);
   w.total = w.acc_off + round_up((size_t)B * H * N * d * 4);
   return w;
 }
@@ -385,8 +384,7 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
   a.dk = dk;
   a.dv = dv;
   a.tile_counter = reinterpret_cast<unsigned int*>(ws + w.sched_off);
-  a.dvec = reinterpret_cast<float*>(ws + w.dvec_off);
-  a.lse2 = reinterpret_cast<float*>(ws + w.lse2_off);
+  a.stats = ws + w.stats_off;
   a.dq_accum = reinterpret_cast<float*>(ws + w.acc_off);
   if (!encode_accum(&a.tm_dq, a.dq_accum, BH, N, d)) return FA_ERR_LAUNCH;
   a.BH = BH;

@@ -9,13 +9,17 @@
 //   dQ = scale dS K,  dK = scale dS^T Q.
 //
 // Three launches:
-//   bwd_pre_kernel   -D and -lse*log2(e) per row, padded to whole 128-row blocks
-//                    (padding rows get 0 and -inf, so their P is exactly 0);
-//                    zeroes the float32 dQ accumulator.
+//   bwd_pre_kernel   -lse/scale and -D per query row, each split into three 16-bit
+//                    terms and written as one operand tile per 128-row block (zeros
+//                    on padding rows, whose Q and dO rows read as zero); zeroes the
+//                    float32 dQ accumulator.
 //   bwd_kv_kernel    persistent over (batch*head, 128-key block) tiles, key/value
 //                    block on the outside, query blocks inside.  Per query block:
-//                      S^T = K Q^T, dP^T = V dO^T            (tcgen05, tensor memory)
-//                      P^T = 2^(S^T scale log2e - lse2), dS^T = P^T o (dP^T - D)
+//                      S^T - lse/scale = K Q^T + 1 (-lse/scale)^T,
+//                      dP^T - D = V dO^T + 1 (-D)^T          (tcgen05, tensor memory;
+//                                        the per-query statistics enter as one more
+//                                        rank-one MMA each, so no thread loads them)
+//                      P^T = 2^((S^T - lse/scale) scale log2e), dS^T = P^T o (dP^T - D)
 //                                        (one thread per key row and query half)
 //                      dV += P^T dO      (P^T read from tensor memory)
 //                      dK += dS^T Q, dQ_part = dS K      (dS^T from shared memory)
@@ -75,8 +79,12 @@ struct BwdCfg {
   static constexpr int kOffDO = kOffQ + kQBufs * kTileBytes;
   static constexpr int kOffDST = kOffDO + kQBufs * kTileBytes;       // 128 x 128 16-bit, K-major SW128
   static constexpr int kOffDQS = kOffDST + 2 * kChunkBytes;          // dQ staging: kDQSChunks x (128 rows x 32 float), SW128
-  static constexpr int kOffStats = kOffDQS + kDQSChunks * kChunkBytes;   // [kQBufs][-lse2[128], -D[128]] float
-  static constexpr int kOffRing = kOffStats + kQBufs * 2 * kRows * 4;   // int[kTileSlots]
+  static constexpr int kOffStats = kOffDQS + kDQSChunks * kChunkBytes;   // [kQBufs] statistics tiles
+  // constant A operands of the rank-one MMAs, three 8-row x 16-byte core matrices
+  // [C | 0 | C], C = (256, 1, 1, 0, 0, 0, 0, 0) in every row: A_L = (C, 0) picks K slots
+  // 0..2 of a statistics tile (-lse/scale), A_D = (0, C) slots 8..10 (-D)
+  static constexpr int kOffCoef = kOffStats + kQBufs * kStatsTileBytes;
+  static constexpr int kOffRing = kOffCoef + 3 * 128;   // int[kTileSlots]
   static constexpr int kOffBar = kOffRing + kTileSlots * 4;
   // barriers
   static constexpr int kKVFull = 0;                   // [kKVBufs]
@@ -119,7 +127,7 @@ template <int D, int DT, bool CAUSAL, int MODE>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                  const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ nlse2, const float* __restrict__ ndvec, float* __restrict__ dq_accum,
+                  const __grid_constant__ CUtensorMap tm_dq, const uint8_t* __restrict__ stats, float* __restrict__ dq_accum,
                   unsigned int* __restrict__ tile_counter,
                   uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, int BHkv, int H, int G, int N, int Npad,
                   float scale,
@@ -178,6 +186,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar(C::kDrain), 1);
     *abort_flag = 0;
     fence_mbar_init();
+  }
+  if (threadIdx.x < 3 * 8) {
+    // the coefficient rows of the rank-one MMAs (16-bit 256 and 1)
+    const uint32_t hi = (DT == 1) ? 0x5C00u : 0x4380u, one = (DT == 1) ? 0x3C00u : 0x3F80u;
+    const bool c = (threadIdx.x >> 3) != 1;
+    *reinterpret_cast<uint4*>(smem + C::kOffCoef + threadIdx.x * 16) =
+        c ? make_uint4(hi | (one << 16), one, 0u, 0u) : make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
   }
   if (warp == 13) {
     tmem_alloc(smem_u32(tmem_holder), 512);
@@ -265,17 +281,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           const uint32_t qdst = smem_u32(smem + C::kOffQ + qs * C::kTileBytes);
           const uint32_t odst = smem_u32(smem + C::kOffDO + qs * C::kTileBytes);
-          const uint32_t stats = smem_u32(smem + C::kOffStats + qs * 2 * kRows * 4);
+          const uint32_t sdst = smem_u32(smem + C::kOffStats + qs * kStatsTileBytes);
           if (elect_one()) {
-            mbar_arrive_expect_tx(bar(C::kQFull + qs), 2 * C::kTileBytes + 2 * kRows * 4);
+            mbar_arrive_expect_tx(bar(C::kQFull + qs), 2 * C::kTileBytes + kStatsTileBytes);
 #pragma unroll
             for (int c = 0; c < C::kChunks; ++c) {
               tma_load_3d(qdst + c * kChunkBytes, &tm_q, bar(C::kQFull + qs), c * 64, qi * kRows, bhq);
               tma_load_3d(odst + c * kChunkBytes, &tm_do, bar(C::kQFull + qs), c * 64, qi * kRows, bhq);
             }
-            const size_t srow = (size_t)bhq * Npad + (size_t)qi * kRows;
-            bulk_load(stats, nlse2 + srow, kRows * 4, bar(C::kQFull + qs));
-            bulk_load(stats + kRows * 4, ndvec + srow, kRows * 4, bar(C::kQFull + qs));
+            const size_t sblock = (size_t)bhq * (Npad / kRows) + qi;
+            bulk_load(sdst, stats + sblock * kStatsTileBytes, kStatsTileBytes, bar(C::kQFull + qs));
           }
           __syncwarp();
         }
@@ -330,6 +345,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           umma_ss(tmem + C::kTmDPT, vd + off, od + off, idesc_s, kk > 0 ? 1u : 0u);
         }
       };
+      // the per-query statistics of step `step` added to every key row: S^T += 1 (-lse/scale)^T
+      // and dP^T += 1 (-D)^T, A = a constant coefficient block (all 8-row groups read the same
+      // core matrix: stride 0), B = the statistics tile (K-major, no swizzle)
+      const uint32_t coef = smem_u32(smem + C::kOffCoef);
+      const uint64_t a_lse = sdesc_noswz(coef, 128, 0);
+      const uint64_t a_d = sdesc_noswz(coef + 128, 128, 0);
+      auto stats_desc = [&](uint32_t step) {
+        return sdesc_noswz(smem_u32(smem + C::kOffStats + (step % C::kQBufs) * kStatsTileBytes), 128, 256);
+      };
+      auto issue_fold_s = [&](uint32_t step) { umma_ss(tmem + C::kTmST, a_lse, stats_desc(step), idesc_s, 1u); };
+      auto issue_fold_dp = [&](uint32_t step) { umma_ss(tmem + C::kTmDPT, a_d, stats_desc(step), idesc_s, 1u); };
       uint32_t s = 0;
       int it = 0;
       bool ok = true;
@@ -354,7 +380,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
         if (elect_one()) {
           issue_st(kbase, qaddr(s));
+          issue_fold_s(s);
           issue_dpt(vbase, oaddr(s));
+          issue_fold_dp(s);
           umma_commit(bar(C::kSFull));
         }
         __syncwarp();
@@ -369,7 +397,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tc_fence_after();
             if (elect_one()) {
               issue_st(kbase, qaddr(s + 1));
+              issue_fold_s(s + 1);
               issue_dpt(vbase, oaddr(s + 1));
+              issue_fold_dp(s + 1);
               umma_commit(bar(C::kSFull));
             }
             __syncwarp();
@@ -433,7 +463,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               break;
             }
             tc_fence_after();
-            if (elect_one()) issue_st(kbase, qaddr(s + 1));
+            if (elect_one()) {
+              issue_st(kbase, qaddr(s + 1));
+              issue_fold_s(s + 1);
+            }
             __syncwarp();
             // dP^T(next) overwrites the dP^T columns that dQ(this) occupies
             if (!wait_warp(bar(C::kDQFree), s & 1, ctl, 0x50c)) {
@@ -443,6 +476,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tc_fence_after();
             if (elect_one()) {
               issue_dpt(vbase, oaddr(s + 1));
+              issue_fold_dp(s + 1);
               umma_commit(bar(C::kSFull));
             }
             __syncwarp();
@@ -481,10 +515,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       bool ok = true;
       for (int g = 0; ok && g < group; ++g)
       for (int qi = q0, j = 0; SPARSE ? j < nq : qi < nb; ++s, ++j, qi = SPARSE ? sparse_q(kb, j) : qi + 1) {
-        const int qs = s % C::kQBufs;
-        bool w = mbar_wait(bar(C::kSFull), s & 1, ctl, 0x601);
-        w = w && mbar_wait(bar(C::kQFull + qs), (s / C::kQBufs) & 1, ctl, 0x602);
-        if (!__all_sync(0xffffffffu, w)) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kSFull), s & 1, ctl, 0x601))) {
           ok = false;
           break;
         }
@@ -499,35 +530,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         reg_fence<64>(pr);
         tc_fence_before();
         mbar_arrive(bar(C::kSTFree));
-        const float4* nl4 = reinterpret_cast<const float4*>(smem + C::kOffStats + qs * 2 * kRows * 4) + 16 * h;
-        const float4* nd4 = nl4 + 32;
         const bool diag = CAUSAL && (qi == kb);
         uint32_t pw[32], dw[32];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {   // 4 query columns per step
-          const float4 L = nl4[k];
-          const float4 Dn = nd4[k];
-#pragma unroll
-          for (int hp = 0; hp < 2; ++hp) {
-            const int e = 4 * k + 2 * hp;          // column inside this half
-            float x0, x1;
-            f2_unpack(ffma2(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2,
-                            hp ? f2_pack(L.z, L.w) : f2_pack(L.x, L.y)),
-                      x0, x1);
-            float p0 = ex2_approx(x0);
-            float p1 = ex2_approx(x1);
-            if (diag) {   // key t is visible to query column c iff t <= c
-              if (64 * h + e < t) p0 = 0.f;
-              if (64 * h + e + 1 < t) p1 = 0.f;
-            }
-            const uint64_t pp = f2_pack(p0, p1);
-            const uint64_t dd = fadd2(f2_pack(__uint_as_float(pr[e]), __uint_as_float(pr[e + 1])),
-                                      hp ? f2_pack(Dn.z, Dn.w) : f2_pack(Dn.x, Dn.y));
-            float d0, d1;
-            f2_unpack(fmul2(pp, dd), d0, d1);
-            pw[e >> 1] = pack2<DT>(p0, p1);
-            dw[e >> 1] = pack2<DT>(d0, d1);
+        for (int e = 0; e < 64; e += 2) {   // two query columns at a time
+          // the tensor memory holds S^T - lse/scale and dP^T - D already
+          float x0, x1;
+          f2_unpack(fmul2(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2), x0, x1);
+          float p0 = ex2_approx(x0);
+          float p1 = ex2_approx(x1);
+          if (diag) {   // key t is visible to query column c iff t <= c
+            if (64 * h + e < t) p0 = 0.f;
+            if (64 * h + e + 1 < t) p1 = 0.f;
           }
+          float d0, d1;
+          f2_unpack(fmul2(f2_pack(p0, p1), f2_pack(__uint_as_float(pr[e]), __uint_as_float(pr[e + 1]))), d0, d1);
+          pw[e >> 1] = pack2<DT>(p0, p1);
+          dw[e >> 1] = pack2<DT>(d0, d1);
         }
         // the previous block's gradient MMAs must be done with P^T and dS^T
         if (!__all_sync(0xffffffffu, s == 0 || mbar_wait(bar(C::kMmaDone), (s - 1) & 1, ctl, 0x603))) {
@@ -668,15 +687,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
-// -D = -rowsum(dO o O) and -lse*log2(e) per row; padded rows -> (0, -inf).  Also
-// zeroes the float32 dQ accumulator.  8 threads per row for d = 64 (16 for d = 128),
-// each reading 16 bytes of O and of dO.
+// x as three 16-bit terms, x = 256 h + m + l to about 24 significant bits: h = x/256
+// rounded, m = the remainder rounded, l = what is left rounded (each remainder is exact in
+// float32).  One 16-byte core-matrix row: (h, m, l, 0, 0, 0, 0, 0).
+template <int DT>
+__device__ __forceinline__ uint4 split3(float x) {
+  const uint32_t h = pack2<DT>(x * (1.0f / 256.0f), 0.0f) & 0xFFFFu;
+  const float r1 = x - 256.0f * unpack2<DT>(h).x;
+  const uint32_t m = pack2<DT>(r1, 0.0f) & 0xFFFFu;
+  const uint32_t l = pack2<DT>(r1 - unpack2<DT>(m).x, 0.0f) & 0xFFFFu;
+  return make_uint4(h | (m << 16), l, 0u, 0u);
+}
+
+// Per query row: -lse/scale and -D = -rowsum(dO o O), written in three 16-bit terms each
+// into the row's line of its block's statistics tile (kStatsTileBytes layout); padding
+// rows get zeros (their Q and dO rows read as zero, so they add nothing whatever P is).
+// Also zeroes the float32 dQ accumulator and the tile counter.  D/8 threads per row
+// (8 for d = 64, 16 for d = 128), each reading 16 bytes of O and of dO.
 template <int D, int DT>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
-                                                      const float* __restrict__ lse, float* __restrict__ ndvec,
-                                                      float* __restrict__ nlse2, float* __restrict__ dq_accum,
+                                                      const float* __restrict__ lse, uint8_t* __restrict__ stats,
+                                                      float* __restrict__ dq_accum,
                                                       unsigned int* __restrict__ tile_counter, int BH, int N, int Npad,
-                                                      size_t accum_elems) {
+                                                      float inv_scale, size_t accum_elems) {
   constexpr int kTPR = D / 8;   // threads per row
   const long long gtid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long row = gtid / kTPR;  // padded row index over BH*Npad
@@ -706,8 +739,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
 #pragma unroll
   for (int off = kTPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (part == 0 && row < rows) {
-    ndvec[row] = valid ? -acc : 0.f;
-    nlse2[row] = valid ? -lse[(size_t)bh * N + n] * kLog2e : -INFINITY;
+    const float nl = valid ? -lse[(size_t)bh * N + n] * inv_scale : 0.f;
+    const float nd = valid ? -acc : 0.f;
+    uint8_t* line = stats + (size_t)(row >> 7) * kStatsTileBytes + ((row & 127) >> 3) * 256 + (row & 7) * 16;
+    *reinterpret_cast<uint4*>(line) = split3<DT>(nl);
+    *reinterpret_cast<uint4*>(line + 128) = split3<DT>(nd);
   }
   // zero the accumulator (grid-stride, 16 bytes per thread per step)
   const size_t n4 = accum_elems / 4;
@@ -745,7 +781,8 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int stages) {
     const size_t accum_elems = (size_t)a.BH * a.N * D;
     cudaError_t e = launch_overlapped(bwd_pre_kernel<D, DT>, (unsigned)blocks, 256, 0, stream,
                                       static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dO), a.lse,
-                                      a.dvec, a.lse2, a.dq_accum, a.tile_counter, a.BH, a.N, a.Npad, accum_elems);
+                                      a.stats, a.dq_accum, a.tile_counter, a.BH, a.N, a.Npad, 1.0f / a.scale,
+                                      accum_elems);
     if (e != cudaSuccess) return e;
   }
   if (stages & kBwdStageKV) {
@@ -761,7 +798,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int stages) {
     const int ntiles = a.BHkv * nb;
     const int grid = ntiles < a.num_sms ? ntiles : a.num_sms;
     e = launch_overlapped(kern, grid, kBwdThreads, C::kSmemBytes, stream, a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dq,
-                          a.lse2, a.dvec, a.dq_accum, a.tile_counter, static_cast<uint16_t*>(a.dk),
+                          a.stats, a.dq_accum, a.tile_counter, static_cast<uint16_t*>(a.dk),
                           static_cast<uint16_t*>(a.dv), a.BHkv, a.H, a.G, a.N, a.Npad, a.scale, a.scale_log2,
                           a.heads_per_group, a.err_word, a.limit_ns);
     if (e != cudaSuccess) return e;

@@ -37,8 +37,8 @@ struct BwdArgs {
   void* dq;
   void* dk;
   void* dv;
-  float* dvec;        // [B*H*Npad]  D = rowsum(dO o O), 0 on padding rows
-  float* lse2;        // [B*H*Npad]  lse * log2(e), +inf on padding rows
+  uint8_t* stats;     // [B*H*Npad/128] 4 KB tiles: -lse/scale and -D per query row as three
+                      // 16-bit terms each, the B operand of the rank-one MMAs (kStatsTileBytes)
   float* dq_accum;    // [B*H*N*d]   float32 dQ partial sums
   unsigned int* tile_counter;  // tiles handed out beyond the first one per CTA
   int BH, N, Npad, d, dtype, causal;   // BH = B*H query heads
@@ -174,6 +174,11 @@ int decode_ctas_per_sm(int d, int dtype, int M);   // resident split-kernel CTAs
 cudaError_t launch_decode(const DecArgs& a, cudaStream_t stream);
 // Backward stages: preprocess (D, lse2, zeroed accumulator), the dK/dV kernel with
 // dQ partial sums, and the dQ conversion.
+// Per 128-row query block the preprocess writes one tile of 128 rows x 16 16-bit values
+// in the tensor core's K-major layout without swizzle (8-row x 16-byte core matrices, the
+// two K halves 128 bytes apart, 8-row groups 256 bytes apart): K slots 0..2 hold
+// -lse/scale split as 256*h + m + l, slots 8..10 hold -D split the same way, the rest 0.
+constexpr int kStatsTileBytes = 4096;
 constexpr int kBwdStagePre = 1;
 constexpr int kBwdStageKV = 2;
 constexpr int kBwdStageDQ = 4;

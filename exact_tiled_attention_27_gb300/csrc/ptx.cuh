@@ -258,6 +258,15 @@ __device__ __forceinline__ uint64_t sdesc_sw64(uint32_t start, uint32_t sbo) {
          (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (4ull << 61);
 }
 
+// Shared-memory matrix descriptor without swizzle (layout type 0): a K-major operand
+// made of 8-row x 16-byte core matrices, `lbo` bytes between core matrices adjacent in
+// K and `sbo` bytes between 8-row groups (0 makes every 8-row group read the same rows).
+__device__ __forceinline__ uint64_t sdesc_noswz(uint32_t start, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((start & 0x3FFFFu) >> 4) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+
 // Instruction descriptor for kind::f8f6f4 with E4M3 A and B (format code 0), both
 // K-major, fp32 accumulation.
 __host__ __device__ constexpr uint32_t idesc_e4m3(uint32_t M, uint32_t N) {

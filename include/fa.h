@@ -115,10 +115,10 @@ int fa_fwd_cross(const void* q, const void* k, const void* v, void* o, float* ls
                  int dtype, void* stream);
 
 /*
- * Bytes of device scratch that fa_bwd needs for these sizes: the per-row
- * D = rowsum(dO o O) and the row log-sum-exp in base 2 (both padded to whole
- * 128-row blocks), plus a float32 dQ accumulator of B*H*N*d elements.
- * Returns 0 for invalid sizes.
+ * Bytes of device scratch that fa_bwd needs for these sizes: per 128-row query
+ * block a 4 KB tile holding -lse/scale and -D = -rowsum(dO o O) of its rows (the
+ * operand of the rank-one products that subtract them on the tensor core), plus a
+ * float32 dQ accumulator of B*H*N*d elements.  Returns 0 for invalid sizes.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 
@@ -287,7 +287,7 @@ int fa_bwd_dq_convert(const void* q, const void* k, const void* v, const void* o
  *
  *   - Sizes whose fa_bwd_workspace_size exceeds that limit are rejected with
  *     FA_ERR_SCRATCH_LIMIT before anything is launched (at d = 64 the limit is
- *     about 8.1 million elements of B*H*N*d).
+ *     about 7.4 million elements of B*H*N*d).
  *   - No cudaMalloc, cudaFree or other allocating call is made.
  *   - The first call on each device looks up the array's device address (with that
  *     device current); make that first call before any stream capture.  The lookup

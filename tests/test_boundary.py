@@ -252,8 +252,8 @@ def test_workspace_size_formula(lib, B, H, N, d):
     def up(x):
         return (x + 255) // 256 * 256
 
-    # tile counter, -D, -lse*log2(e) (padded rows), float32 dQ accumulator
-    expect = 256 + 2 * up(B * H * npad * 4) + up(B * H * N * d * 4)
+    # tile counter, one 4 KB statistics tile per 128-row query block, float32 dQ accumulator
+    expect = 256 + up(B * H * (npad // 128) * 4096) + up(B * H * N * d * 4)
     assert lib.fa_bwd_workspace_size(B, H, N, d) == expect
     assert lib.fa_bwd_workspace_size(0, H, N, d) == 0
     assert lib.fa_bwd_workspace_size(B, H, N, 80) == 0
