@@ -113,15 +113,15 @@ bool encode_bhnd(CUtensorMap* m, const void* base, int BH, int N, int d, int dty
   return r == CUDA_SUCCESS;
 }
 
-// 3-D map over the contiguous (B*H, N, d) float32 dQ accumulator: box of 128 rows x
-// 32 floats (one 128-byte swizzle row per tensor row), used for bulk reductions.
+// 3-D map over the contiguous (B*H, N, d) float32 dQ accumulator: box of 32 rows x
+// 16 floats (one 64-byte swizzle row per tensor row), used for bulk reductions.
 bool encode_accum(CUtensorMap* m, void* base, int BH, int N, int d) {
   const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
   const cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)N * d * 4};
-  const cuuint32_t box[3] = {32, 128, 1};
+  const cuuint32_t box[3] = {16, 32, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }

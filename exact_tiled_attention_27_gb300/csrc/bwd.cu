@@ -69,17 +69,20 @@ struct BwdCfg {
   static constexpr bool kEarly = (D == 64);          // next S^T / dP^T issued before this block's gradients
   static constexpr int kKVBufs = (D == 64) ? 2 : 1;
   static constexpr int kQBufs = (D == 64) ? 3 : 1;
-  // dQ staging chunks of 128 rows x 32 floats: d = 64 stages its two chunks one after the
-  // other through one buffer, which leaves room for the third Q/dO buffer
-  static constexpr int kDQSChunks = (D == 64) ? 1 : 2;
+  // dQ staging: every warp of the dQ warpgroup stages its 32 rows in chunks of 16 floats
+  // (2 KB, 64-byte swizzle) through a ring of its own, so that a chunk is written while
+  // the bulk reductions of the previous ones still read theirs (16 KB at d = 64, which
+  // leaves room for the third Q/dO buffer; 32 KB at d = 128)
+  static constexpr int kDQRing = (D == 64) ? 2 : 4;
+  static constexpr int kDQChunkBytes = 32 * 16 * 4;
   static_assert(!kEarly || kQBufs >= 2, "early issue needs two Q/dO buffers");
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kKVBufs * kTileBytes;
   static constexpr int kOffQ = kOffV + kKVBufs * kTileBytes;
   static constexpr int kOffDO = kOffQ + kQBufs * kTileBytes;
   static constexpr int kOffDST = kOffDO + kQBufs * kTileBytes;       // 128 x 128 16-bit, K-major SW128
-  static constexpr int kOffDQS = kOffDST + 2 * kChunkBytes;          // dQ staging: kDQSChunks x (128 rows x 32 float), SW128
-  static constexpr int kOffStats = kOffDQS + kDQSChunks * kChunkBytes;   // [kQBufs] statistics tiles
+  static constexpr int kOffDQS = kOffDST + 2 * kChunkBytes;          // dQ staging: [4 warps][kDQRing] chunks
+  static constexpr int kOffStats = kOffDQS + 4 * kDQRing * kDQChunkBytes;   // [kQBufs] statistics tiles
   // constant A operands of the rank-one MMAs, three 8-row x 16-byte core matrices
   // [C | 0 | C], C = (256, 1, 1, 0, 0, 0, 0, 0) in every row: A_L = (C, 0) picks K slots
   // 0..2 of a statistics tile (-lse/scale), A_D = (0, C) slots 8..10 (-D)
@@ -569,6 +572,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------ dQ warpgroup: dQ reduction, dK/dV epilogue
     regs_dec<kDqRegs>();
     const int u = threadIdx.x - 256;
+    const int dq_warp = warp - 8;          // rows 32*dq_warp .. +31 of each query block
+    const int lane = threadIdx.x & 31;
+    uint32_t dq_chunks = 0;                // chunks this warp has staged (its ring position)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     // dK (times scale) and dV of the key block, read out of tensor memory; the columns
     // are handed back to the MMA warp as soon as the last of them is in registers
@@ -642,29 +648,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_arrive(bar(C::kDQFree));
           }
 #pragma unroll
-          for (int c0 = 0; c0 < 2; c0 += C::kDQSChunks) {   // one or two staging rounds
+          for (int q = 0; q < 4; ++q) {   // chunks of 16 columns
+            uint8_t* box = smem + C::kOffDQS + (dq_warp * C::kDQRing + dq_chunks % C::kDQRing) * C::kDQChunkBytes;
+            // the reduction that last read this buffer must be done reading it
+            if (lane == 0 && dq_chunks >= (uint32_t)C::kDQRing) bulk_wait_read<C::kDQRing - 1>();
+            __syncwarp();
+            const uint32_t* src = r[q >> 1] + (q & 1) * 16;
 #pragma unroll
-            for (int cc = 0; cc < C::kDQSChunks; ++cc) {
-              uint8_t* box = smem + C::kOffDQS + cc * kChunkBytes;
-#pragma unroll
-              for (int v = 0; v < 8; ++v)
-                *reinterpret_cast<uint4*>(box + sw128_offset(u, v)) = make_uint4(
-                    r[c0 + cc][4 * v], r[c0 + cc][4 * v + 1], r[c0 + cc][4 * v + 2], r[c0 + cc][4 * v + 3]);
-            }
+            for (int v = 0; v < 4; ++v)   // 64-byte rows, 16-byte units swizzled by (row / 2) mod 4
+              *reinterpret_cast<uint4*>(box + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4)) =
+                  make_uint4(src[4 * v], src[4 * v + 1], src[4 * v + 2], src[4 * v + 3]);
             fence_proxy_async_smem();
-            named_bar_sync(1, 128);
-            if (warp == 8) {
-              if (elect_one()) {
-#pragma unroll
-                for (int cc = 0; cc < C::kDQSChunks; ++cc)
-                  tma_reduce_add_3d(&tm_dq, smem_u32(smem + C::kOffDQS + cc * kChunkBytes),
-                                    (half * 2 + c0 + cc) * 32, qi * kRows, bhq);
-                bulk_commit_group();
-                bulk_wait_read_all();   // the staging tile may be overwritten after this
-              }
-              __syncwarp();
+            __syncwarp();
+            if (lane == 0) {
+              tma_reduce_add_3d(&tm_dq, smem_u32(box), half * 64 + q * 16, qi * kRows + 32 * dq_warp, bhq);
+              bulk_commit_group();
             }
-            named_bar_sync(1, 128);
+            ++dq_chunks;
           }
         }
       }
@@ -672,11 +672,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!ok) break;
       if (!C::kEarly && !write_dkdv(it, kb, bh)) break;
     }
-    // every bulk reduction issued by this warpgroup must complete before the CTA exits
-    if (warp == 8) {
-      if (elect_one()) bulk_wait_all();
-      __syncwarp();
-    }
+    // every bulk reduction issued by this warp must complete before the CTA exits
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();

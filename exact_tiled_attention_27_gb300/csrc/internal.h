@@ -30,7 +30,7 @@ struct FwdArgs {
 struct BwdArgs {
   CUtensorMap tm_q, tm_do;       // {d, N, B*H}
   CUtensorMap tm_k, tm_v;        // {d, N, B*Hkv}
-  CUtensorMap tm_dq;  // 3-D map {d, N, B*H} over the float32 dQ accumulator, box {32, 128, 1}
+  CUtensorMap tm_dq;  // 3-D map {d, N, B*H} over the float32 dQ accumulator, box {16, 32, 1}
   const void* o;
   const void* dO;
   const float* lse;
