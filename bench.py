@@ -591,6 +591,7 @@ def run_extra(args, w, local_rank):
     elif w["kind"] == "decode":
         nbytes = 2 * B * Hkv * Nk * d * 2 + 2 * B * H * Nq * d * 2 + B * H * Nq * 4
         gbs = nbytes / (t * 1e-3) / 1e9
+        dec_kernel = "decode_tma_kernel" if d == 128 else "decode_split_kernel"
         hbm, src = 6800.0, "fallback"
         pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
         if os.path.exists(pk):
@@ -598,10 +599,10 @@ def run_extra(args, w, local_rank):
                 hbm, src = float(json.load(f)["hbm_gbs"]), "measured"
         res.update({"metric": "decode: bytes of K, V, Q, O and lse moved per second", "value": round(gbs, 1),
                     "unit": "GB/s",
-                    "roofline": {"bound": "hbm", "kernel": "decode_split_kernel_d64|d128", "achieved": round(gbs, 1),
+                    "roofline": {"bound": "hbm", "kernel": dec_kernel, "achieved": round(gbs, 1),
                                  "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
                                  "peak_source": f"{src} copy bandwidth",
-                                 "traffic": traffic_for("decode_split_kernel", args.workload)}})
+                                 "traffic": traffic_for(dec_kernel, args.workload)}})
     else:
         pairs = H * B * cross_visible_pairs(Nq, Nk, bool(causal))
         f = pairs * d * (4 + (10 if w["backward"] else 0))
@@ -620,6 +621,7 @@ def run_extra(args, w, local_rank):
 
 
 KERNEL_SOURCE = {"fwd_kernel": "fwd.cu", "bwd_kv_kernel": "bwd.cu", "decode_split_kernel": "decode.cu",
+                 "decode_tma_kernel": "decode.cu",
                  "fwd_fp8_kernel": "fwd_fp8.cu"}
 
 

@@ -113,6 +113,20 @@ bool encode_bhnd(CUtensorMap* m, const void* base, int BH, int N, int d, int dty
   return r == CUDA_SUCCESS;
 }
 
+// 3-D map over a contiguous (B*H, N, d) 16-bit tensor with a box of `rows` rows x 64
+// elements, 128-byte swizzle (the decode kernel's 32-key stages).
+bool encode_bhnd_rows(CUtensorMap* m, const void* base, int BH, int N, int d, int dtype, int rows) {
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(m, dtype == FA_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                              3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 3-D map over the contiguous (B*H, N, d) float32 dQ accumulator: box of 32 rows x
 // 16 floats (one 64-byte swizzle row per tensor row), used for bulk reductions.
 bool encode_accum(CUtensorMap* m, void* base, int BH, int N, int d) {
@@ -498,19 +512,46 @@ int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, 
   a.dtype = dtype;
   a.causal = causal ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
-  // as many ranges as fill every SM's resident CTA slots in one wave (a second, partial
-  // wave would run alone at the end), each range a whole number of CTA steps
   const int smax = decode_max_splits(Nk);
-  int per_sm = decode_ctas_per_sm(d, dtype, a.M);
-  if (per_sm < 1) per_sm = 1;
-  long long want = (long long)per_sm * dev->num_sms / a.BHkv;
-  if (want < 1) want = 1;
-  if (want > smax) want = smax;
-  const int kps = decode_keys_per_step(d);
-  int chunk = (int)((Nk + want - 1) / want);
-  chunk = (chunk + kps - 1) / kps * kps;
-  a.chunk = chunk;
-  a.S = (Nk + chunk - 1) / chunk;
+  // d = 128: the TMA-fed kernel, one CTA per SM; the number of ranges minimises the
+  // makespan estimate (waves of CTAs x stages per range, plus a few stages of start-up)
+  a.tma = d == 128 ? 1 : 0;
+  if (a.tma) {
+    a.err_word = dev->err_word;
+    a.limit_ns = kWaitLimitNs;
+    if (!encode_bhnd_rows(&a.tm_k, k, a.BHkv, Nk, d, dtype, kDecodeTmaKeys) ||
+        !encode_bhnd_rows(&a.tm_v, v, a.BHkv, Nk, d, dtype, kDecodeTmaKeys))
+      return FA_ERR_LAUNCH;
+    const long long stages = (Nk + kDecodeTmaKeys - 1) / kDecodeTmaKeys;
+    long long best = -1;
+    int best_s = 1;
+    for (int sp = 1; sp <= smax; ++sp) {
+      const long long per = (stages + sp - 1) / sp;
+      if (sp > 1 && per < 8) break;   // ranges of at least 8 stages
+      const long long waves = ((long long)a.BHkv * sp + dev->num_sms - 1) / dev->num_sms;
+      const long long cost = waves * (per + 4);
+      if (best < 0 || cost < best) {
+        best = cost;
+        best_s = sp;
+      }
+    }
+    const long long per = (stages + best_s - 1) / best_s;
+    a.chunk = (int)(per * kDecodeTmaKeys);
+    a.S = (Nk + a.chunk - 1) / a.chunk;
+  } else {
+    // as many ranges as fill every SM's resident CTA slots in one wave (a second, partial
+    // wave would run alone at the end), each range a whole number of CTA steps
+    int per_sm = decode_ctas_per_sm(d, dtype, a.M);
+    if (per_sm < 1) per_sm = 1;
+    long long want = (long long)per_sm * dev->num_sms / a.BHkv;
+    if (want < 1) want = 1;
+    if (want > smax) want = smax;
+    const int kps = decode_keys_per_step(d);
+    int chunk = (int)((Nk + want - 1) / want);
+    chunk = (chunk + kps - 1) / kps * kps;
+    a.chunk = chunk;
+    a.S = (Nk + chunk - 1) / chunk;
+  }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const size_t rows = (size_t)a.S * a.BHkv * a.M;
   a.opart = a.S > 1 ? reinterpret_cast<float*>(ws) : nullptr;

@@ -33,6 +33,13 @@ CASES = [
     (1, 2, 1, 4, 20000, 128, "fp16", True),    # 8 rows, 78 ranges
     (1, 1, 1, 8, 5, 64, "bf16", True),         # Nk < Nq: three rows see no key
     (3, 6, 3, 2, 1111, 64, "fp16", False),
+    # d = 128 runs the TMA-fed kernel: partial stages, the mask, rows that see no key,
+    # ranges of many stages
+    (1, 4, 4, 1, 100, 128, "fp16", True),
+    (1, 2, 2, 3, 777, 128, "bf16", True),
+    (1, 1, 1, 8, 5, 128, "bf16", True),
+    (3, 6, 3, 2, 1111, 128, "fp16", False),
+    (2, 8, 8, 1, 40000, 128, "bf16", True),
 ]
 
 
@@ -53,10 +60,11 @@ def test_decode_matches_oracle(B, H, Hkv, Nq, Nk, d, dtype, causal):
     G.check_forward(o[live], lse[live], o_ref[live], lse_ref[live], f"decode B{B} H{H}/{Hkv} {Nq}x{Nk} d{d}", dtype)
 
 
-def test_decode_agrees_with_tile_forward_and_is_repeatable():
-    c = make_cross_case(4, 16, 2, 1, 9000, 64, "bf16", True, workload_index=211)
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_agrees_with_tile_forward_and_is_repeatable(d):
+    c = make_cross_case(4, 16, 2, 1, 9000, d, "bf16", True, workload_index=211)
     q, k, v = (G.to_device(getattr(c, n), "bf16") for n in ("q", "k", "v"))
-    ws = torch.empty(decode_workspace_size(4, 16, 2, 1, 9000, 64), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(decode_workspace_size(4, 16, 2, 1, 9000, d), dtype=torch.uint8, device="cuda")
     o1, l1 = decode(q, k, v, causal=True, workspace=ws)
     o2, l2 = decode(q, k, v, causal=True, workspace=ws)
     o3, l3 = forward_cross(q, k, v, causal=True)
