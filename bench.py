@@ -591,7 +591,7 @@ def run_extra(args, w, local_rank):
     elif w["kind"] == "decode":
         nbytes = 2 * B * Hkv * Nk * d * 2 + 2 * B * H * Nq * d * 2 + B * H * Nq * 4
         gbs = nbytes / (t * 1e-3) / 1e9
-        dec_kernel = "decode_tma_kernel" if d == 128 else "decode_split_kernel"
+        dec_kernel = "decode_split_kernel"
         hbm, src = 6800.0, "fallback"
         pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
         if os.path.exists(pk):
@@ -621,7 +621,6 @@ def run_extra(args, w, local_rank):
 
 
 KERNEL_SOURCE = {"fwd_kernel": "fwd.cu", "bwd_kv_kernel": "bwd.cu", "decode_split_kernel": "decode.cu",
-                 "decode_tma_kernel": "decode.cu",
                  "fwd_fp8_kernel": "fwd_fp8.cu"}
 
 

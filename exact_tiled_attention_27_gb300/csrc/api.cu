@@ -512,46 +512,31 @@ int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, 
   a.dtype = dtype;
   a.causal = causal ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.err_word = dev->err_word;
+  a.limit_ns = kWaitLimitNs;
+  if (!encode_bhnd_rows(&a.tm_k, k, a.BHkv, Nk, d, dtype, kDecodeTmaKeys) ||
+      !encode_bhnd_rows(&a.tm_v, v, a.BHkv, Nk, d, dtype, kDecodeTmaKeys))
+    return FA_ERR_LAUNCH;
+  // One CTA per SM at a time.  The number of ranges minimises the makespan estimate
+  // (waves of CTAs x stages per range, plus a few stages of start-up), with ranges of at
+  // least 8 stages.
   const int smax = decode_max_splits(Nk);
-  // d = 128: the TMA-fed kernel, one CTA per SM; the number of ranges minimises the
-  // makespan estimate (waves of CTAs x stages per range, plus a few stages of start-up)
-  a.tma = d == 128 ? 1 : 0;
-  if (a.tma) {
-    a.err_word = dev->err_word;
-    a.limit_ns = kWaitLimitNs;
-    if (!encode_bhnd_rows(&a.tm_k, k, a.BHkv, Nk, d, dtype, kDecodeTmaKeys) ||
-        !encode_bhnd_rows(&a.tm_v, v, a.BHkv, Nk, d, dtype, kDecodeTmaKeys))
-      return FA_ERR_LAUNCH;
-    const long long stages = (Nk + kDecodeTmaKeys - 1) / kDecodeTmaKeys;
-    long long best = -1;
-    int best_s = 1;
-    for (int sp = 1; sp <= smax; ++sp) {
-      const long long per = (stages + sp - 1) / sp;
-      if (sp > 1 && per < 8) break;   // ranges of at least 8 stages
-      const long long waves = ((long long)a.BHkv * sp + dev->num_sms - 1) / dev->num_sms;
-      const long long cost = waves * (per + 4);
-      if (best < 0 || cost < best) {
-        best = cost;
-        best_s = sp;
-      }
+  const long long stages = (Nk + kDecodeTmaKeys - 1) / kDecodeTmaKeys;
+  long long best = -1;
+  int best_s = 1;
+  for (int sp = 1; sp <= smax; ++sp) {
+    const long long per = (stages + sp - 1) / sp;
+    if (sp > 1 && per < 8) break;
+    const long long waves = ((long long)a.BHkv * sp + dev->num_sms - 1) / dev->num_sms;
+    const long long cost = waves * (per + 4);
+    if (best < 0 || cost < best) {
+      best = cost;
+      best_s = sp;
     }
-    const long long per = (stages + best_s - 1) / best_s;
-    a.chunk = (int)(per * kDecodeTmaKeys);
-    a.S = (Nk + a.chunk - 1) / a.chunk;
-  } else {
-    // as many ranges as fill every SM's resident CTA slots in one wave (a second, partial
-    // wave would run alone at the end), each range a whole number of CTA steps
-    int per_sm = decode_ctas_per_sm(d, dtype, a.M);
-    if (per_sm < 1) per_sm = 1;
-    long long want = (long long)per_sm * dev->num_sms / a.BHkv;
-    if (want < 1) want = 1;
-    if (want > smax) want = smax;
-    const int kps = decode_keys_per_step(d);
-    int chunk = (int)((Nk + want - 1) / want);
-    chunk = (chunk + kps - 1) / kps * kps;
-    a.chunk = chunk;
-    a.S = (Nk + chunk - 1) / chunk;
   }
+  const long long per = (stages + best_s - 1) / best_s;
+  a.chunk = (int)(per * kDecodeTmaKeys);
+  a.S = (Nk + a.chunk - 1) / a.chunk;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const size_t rows = (size_t)a.S * a.BHkv * a.M;
   a.opart = a.S > 1 ? reinterpret_cast<float*>(ws) : nullptr;

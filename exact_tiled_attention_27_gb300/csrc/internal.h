@@ -167,15 +167,12 @@ struct DecArgs {
   float* lpart;       // [S, B*Hkv, M] float32 natural-log lse of each range
   int BHkv, H, Hkv, Nq, Nk, M, S, chunk, d, dtype, causal;
   float scale_log2;
-  int tma;            // the TMA-fed split kernel (tm_k, tm_v, err_word, limit_ns used)
   CUtensorMap tm_k, tm_v;   // 3-D maps {d, Nk, B*Hkv}, box {64, 32, 1}, 128-byte swizzle
-  unsigned int* err_word;
+  unsigned int* err_word;   // bounded waits: error word and limit
   uint64_t limit_ns;
 };
 constexpr int kDecodeMaxRows = 8;
-constexpr int kDecodeTmaKeys = 32;   // keys per stage of the TMA-fed split kernel
-int decode_keys_per_step(int d);
-int decode_ctas_per_sm(int d, int dtype, int M);   // resident split-kernel CTAs per SM, 0 on error
+constexpr int kDecodeTmaKeys = 32;   // keys per stage of the split kernel
 cudaError_t launch_decode(const DecArgs& a, cudaStream_t stream);
 // Backward stages: preprocess (D, lse2, zeroed accumulator), the dK/dV kernel with
 // dQ partial sums, and the dQ conversion.
