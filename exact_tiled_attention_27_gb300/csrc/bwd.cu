@@ -533,19 +533,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         reg_fence<64>(pr);
         tc_fence_before();
         mbar_arrive(bar(C::kSTFree));
-        const bool diag = CAUSAL && (qi == kb);
+        if (CAUSAL && qi == kb) {   // key t is visible to query column c iff t <= c: P = 0 elsewhere
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (64 * h + e < t) sr[e] = 0xFF800000u;   // -inf: 2^-inf = 0, and dS = 0 * (dP - D) = 0
+        }
         uint32_t pw[32], dw[32];
 #pragma unroll
         for (int e = 0; e < 64; e += 2) {   // two query columns at a time
           // the tensor memory holds S^T - lse/scale and dP^T - D already
           float x0, x1;
           f2_unpack(fmul2(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2), x0, x1);
-          float p0 = ex2_approx(x0);
-          float p1 = ex2_approx(x1);
-          if (diag) {   // key t is visible to query column c iff t <= c
-            if (64 * h + e < t) p0 = 0.f;
-            if (64 * h + e + 1 < t) p1 = 0.f;
-          }
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
           float d0, d1;
           f2_unpack(fmul2(f2_pack(p0, p1), f2_pack(__uint_as_float(pr[e]), __uint_as_float(pr[e + 1]))), d0, d1);
           pw[e >> 1] = pack2<DT>(p0, p1);
