@@ -129,13 +129,14 @@ bool encode_bhnd_rows(CUtensorMap* m, const void* base, int BH, int N, int d, in
 
 // 3-D map over the contiguous (B*H, N, d) float32 dQ accumulator: box of 32 rows x
 // 16 floats (one 64-byte swizzle row per tensor row), used for bulk reductions.
-bool encode_accum(CUtensorMap* m, void* base, int BH, int N, int d) {
+bool encode_accum(CUtensorMap* m, void* base, int BH, int N, int d, bool wide) {
   const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
   const cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)N * d * 4};
-  const cuuint32_t box[3] = {16, 32, 1};
+  const cuuint32_t box[3] = {wide ? 32u : 16u, 32, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              wide ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -400,7 +401,12 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
   a.tile_counter = reinterpret_cast<unsigned int*>(ws + w.sched_off);
   a.stats = ws + w.stats_off;
   a.dq_accum = reinterpret_cast<float*>(ws + w.acc_off);
-  if (!encode_accum(&a.tm_dq, a.dq_accum, BH, N, d)) return FA_ERR_LAUNCH;
+  // d = 64, dense: long tiles stage dQ in 32-column chunks (half as many bulk reductions,
+  // one staging chunk per warp); short tiles keep 16-column chunks, two per warp in flight
+  const int nb = (N + 127) / 128;
+  const int steps_per_tile = causal ? (nb + 1) / 2 : nb;
+  a.wide_dq = (d == 64 && pattern == 0 && Hkv == H && steps_per_tile >= 24) ? 1 : 0;
+  if (!encode_accum(&a.tm_dq, a.dq_accum, BH, N, d, a.wide_dq != 0)) return FA_ERR_LAUNCH;
   a.BH = BH;
   a.BHkv = B * Hkv;
   a.H = H;

@@ -62,7 +62,7 @@ static_assert((2 * kDsRegs + kDqRegs + kCtlRegs) * 128 <= kBwdLaunchRegs * kBwdT
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kTileSlots = 4;   // tile numbers the producer may publish ahead of the slowest role
 
-template <int D>
+template <int D, bool WIDE = false>
 struct BwdCfg {
   static constexpr int kChunks = D / 64;
   static constexpr int kTileBytes = kRows * D * 2;
@@ -73,8 +73,12 @@ struct BwdCfg {
   // (2 KB, 64-byte swizzle) through a ring of its own, so that a chunk is written while
   // the bulk reductions of the previous ones still read theirs (16 KB at d = 64, which
   // leaves room for the third Q/dO buffer; 32 KB at d = 128)
-  static constexpr int kDQRing = (D == 64) ? 2 : 4;
-  static constexpr int kDQChunkBytes = 32 * 16 * 4;
+  // (WIDE, d = 64 only: 32 rows x 32 floats, 4 KB, 128-byte swizzle, one per warp: half as
+  // many bulk reductions, which measured faster on long tiles and slower on short ones)
+  static_assert(!WIDE || D == 64, "wide dQ staging is a d = 64 layout");
+  static constexpr int kDQCols = WIDE ? 32 : 16;
+  static constexpr int kDQRing = WIDE ? 1 : ((D == 64) ? 2 : 4);
+  static constexpr int kDQChunkBytes = 32 * kDQCols * 4;
   static_assert(!kEarly || kQBufs >= 2, "early issue needs two Q/dO buffers");
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kKVBufs * kTileBytes;
@@ -125,8 +129,9 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int u) {
 
 // MODE 1 (GQA): key/value heads shared by groups of G > 1 query heads (fa_bwd_gqa).
 // MODE 2 (SPARSE): the butterfly block pattern (fa_bwd_sparse): a key block visits the
-// query blocks of its pair's linked pairs.  MODE 0: G = 1, dense.
-template <int D, int DT, bool CAUSAL, int MODE>
+// query blocks of its pair's linked pairs.  MODE 0: G = 1, dense.  WIDE: 32-column dQ
+// staging chunks (d = 64).
+template <int D, int DT, bool CAUSAL, int MODE, bool WIDE>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -135,7 +140,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                   uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, int BHkv, int H, int G, int N, int Npad,
                   float scale,
                   float scale_log2, int hg, unsigned int* err_word, uint64_t limit_ns) {
-  using C = BwdCfg<D>;
+  using C = BwdCfg<D, WIDE>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned base, derived from the __shared__ array by pointer arithmetic so
   // that every access through it stays a shared-memory access (not a generic one)
@@ -648,20 +653,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_arrive(bar(C::kDQFree));
           }
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {   // chunks of 16 columns
+          for (int q = 0; q < 64 / C::kDQCols; ++q) {   // chunks of kDQCols columns
             uint8_t* box = smem + C::kOffDQS + (dq_warp * C::kDQRing + dq_chunks % C::kDQRing) * C::kDQChunkBytes;
             // the reduction that last read this buffer must be done reading it
             if (lane == 0 && dq_chunks >= (uint32_t)C::kDQRing) bulk_wait_read<C::kDQRing - 1>();
             __syncwarp();
-            const uint32_t* src = r[q >> 1] + (q & 1) * 16;
+            if constexpr (WIDE) {
+              const uint32_t* src = r[q];
 #pragma unroll
-            for (int v = 0; v < 4; ++v)   // 64-byte rows, 16-byte units swizzled by (row / 2) mod 4
-              *reinterpret_cast<uint4*>(box + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4)) =
-                  make_uint4(src[4 * v], src[4 * v + 1], src[4 * v + 2], src[4 * v + 3]);
+              for (int v = 0; v < 8; ++v)   // 128-byte rows, 16-byte units swizzled by row mod 8
+                *reinterpret_cast<uint4*>(box + lane * 128 + ((v ^ (lane & 7)) << 4)) =
+                    make_uint4(src[4 * v], src[4 * v + 1], src[4 * v + 2], src[4 * v + 3]);
+            } else {
+              const uint32_t* src = r[q >> 1] + (q & 1) * 16;
+#pragma unroll
+              for (int v = 0; v < 4; ++v)   // 64-byte rows, 16-byte units swizzled by (row / 2) mod 4
+                *reinterpret_cast<uint4*>(box + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4)) =
+                    make_uint4(src[4 * v], src[4 * v + 1], src[4 * v + 2], src[4 * v + 3]);
+            }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_reduce_add_3d(&tm_dq, smem_u32(box), half * 64 + q * 16, qi * kRows + 32 * dq_warp, bhq);
+              tma_reduce_add_3d(&tm_dq, smem_u32(box), half * 64 + q * C::kDQCols, qi * kRows + 32 * dq_warp, bhq);
               bulk_commit_group();
             }
             ++dq_chunks;
@@ -767,9 +780,28 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ a
   }
 }
 
+template <int D, int DT, bool CAUSAL, int MODE, bool WIDE>
+cudaError_t launch_kv_t(const BwdArgs& a, cudaStream_t stream) {
+  using C = BwdCfg<D, WIDE>;
+  auto kern = bwd_kv_kernel<D, DT, CAUSAL, MODE, WIDE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  // the setmaxnreg split inside the kernel must fit what the launch provides
+  cudaFuncAttributes attr;
+  e = cudaFuncGetAttributes(&attr, kern);
+  if (e != cudaSuccess) return e;
+  if (attr.numRegs * kBwdThreads < (2 * kDsRegs + kDqRegs + kCtlRegs) * 128) return cudaErrorInvalidConfiguration;
+  const int nb = (a.N + kRows - 1) / kRows;
+  const int ntiles = a.BHkv * nb;
+  const int grid = ntiles < a.num_sms ? ntiles : a.num_sms;
+  return launch_overlapped(kern, grid, kBwdThreads, C::kSmemBytes, stream, a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dq,
+                           a.stats, a.dq_accum, a.tile_counter, static_cast<uint16_t*>(a.dk),
+                           static_cast<uint16_t*>(a.dv), a.BHkv, a.H, a.G, a.N, a.Npad, a.scale, a.scale_log2,
+                           a.heads_per_group, a.err_word, a.limit_ns);
+}
+
 template <int D, int DT, bool CAUSAL, int MODE>
 cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int stages) {
-  using C = BwdCfg<D>;
   if (stages & kBwdStagePre) {
     constexpr int kTPR = D / 8;
     const long long threads = (long long)a.BH * a.Npad * kTPR;
@@ -784,21 +816,11 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int stages) {
     if (e != cudaSuccess) return e;
   }
   if (stages & kBwdStageKV) {
-    auto kern = bwd_kv_kernel<D, DT, CAUSAL, MODE>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    // the setmaxnreg split inside the kernel must fit what the launch provides
-    cudaFuncAttributes attr;
-    e = cudaFuncGetAttributes(&attr, kern);
-    if (e != cudaSuccess) return e;
-    if (attr.numRegs * kBwdThreads < (2 * kDsRegs + kDqRegs + kCtlRegs) * 128) return cudaErrorInvalidConfiguration;
-    const int nb = (a.N + kRows - 1) / kRows;
-    const int ntiles = a.BHkv * nb;
-    const int grid = ntiles < a.num_sms ? ntiles : a.num_sms;
-    e = launch_overlapped(kern, grid, kBwdThreads, C::kSmemBytes, stream, a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dq,
-                          a.stats, a.dq_accum, a.tile_counter, static_cast<uint16_t*>(a.dk),
-                          static_cast<uint16_t*>(a.dv), a.BHkv, a.H, a.G, a.N, a.Npad, a.scale, a.scale_log2,
-                          a.heads_per_group, a.err_word, a.limit_ns);
+    cudaError_t e;
+    if constexpr (D == 64 && MODE == 0)
+      e = a.wide_dq ? launch_kv_t<D, DT, CAUSAL, MODE, true>(a, stream) : launch_kv_t<D, DT, CAUSAL, MODE, false>(a, stream);
+    else
+      e = launch_kv_t<D, DT, CAUSAL, MODE, false>(a, stream);
     if (e != cudaSuccess) return e;
   }
   if (stages & kBwdStageDQ) {

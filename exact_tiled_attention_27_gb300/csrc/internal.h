@@ -31,6 +31,7 @@ struct BwdArgs {
   CUtensorMap tm_q, tm_do;       // {d, N, B*H}
   CUtensorMap tm_k, tm_v;        // {d, N, B*Hkv}
   CUtensorMap tm_dq;  // 3-D map {d, N, B*H} over the float32 dQ accumulator, box {16, 32, 1}
+                      // (64-byte swizzle), or {32, 32, 1} (128-byte swizzle) when wide_dq
   const void* o;
   const void* dO;
   const float* lse;
@@ -49,6 +50,7 @@ struct BwdArgs {
   uint64_t limit_ns;
   int num_sms;
   int heads_per_group;           // tile order: see group_order
+  int wide_dq;                   // d = 64, dense: dQ staged in 32-column chunks (one per warp)
 };
 
 // Order of the persistent work tiles.  A head (b, h) has `units` tiles, unit 0 the

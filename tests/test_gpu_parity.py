@@ -80,3 +80,11 @@ def test_large_logits_do_not_overflow():
     """Scores of several hundred: the running maximum keeps exp finite."""
     case = make_case(1, 2, 256, 64, "fp16", False, scale=4.0, workload_index=94, mult=3.0)
     run_and_check(case, False, "scale=4 x3")
+
+
+@pytest.mark.parametrize("N,causal,dtype", [(3001, False, "bf16"), (6001, True, "fp16")])
+def test_long_tiles_wide_dq_staging(N, causal, dtype):
+    """d = 64 with 24 or more query blocks per key tile: the backward stages dQ in
+    32-column chunks (one per warp) instead of 16-column ones; ragged last block."""
+    case = make_case(1, 2, N, 64, dtype, causal, workload_index=95, length_index=N % 83)
+    run_and_check(case, True, f"wide dQ N={N} causal={causal} {dtype}")
