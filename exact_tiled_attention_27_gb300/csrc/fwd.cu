@@ -96,7 +96,8 @@ struct FwdCfg {
   static constexpr int kPHalf = kSFull + 2;                 // [2] first 64 keys of P written
   static constexpr int kPFull = kPHalf + 2;                 // [2]
   static constexpr int kOFull = kPFull + 2;                 // [2]
-  static constexpr int kOEmpty = kOFull + 2;                // [2]
+  static constexpr int kP2Free = kOFull + 2;                // [2] P.V of the second 64 keys done (d = 64)
+  static constexpr int kOEmpty = kP2Free + 2;               // [2]
   static constexpr int kDrain = kOEmpty + 2;
   static constexpr int kNumBars = kDrain + 1;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;   // + alignment slack
@@ -105,12 +106,18 @@ struct FwdCfg {
   // P_t occupies the first 64 columns of S_t; O_t (kPVN columns) follows the S buffers
   __host__ __device__ static constexpr uint32_t tm_p(int t) { return t * 128; }
   __host__ __device__ static constexpr uint32_t tm_o(int t) { return 256 + t * 128; }
+  // d = 64: P of the second 64 keys goes to 32 columns of its own after O_t's 80, so that
+  // with single-block tiles the next scores may overwrite S_t as soon as the first half's
+  // P.V has read it (d = 128 has no columns to spare: both halves of P stay in S_t)
+  static constexpr bool kP2 = (D == 64);
+  __host__ __device__ static constexpr uint32_t tm_p2(int t) { return kP2 ? 256 + t * 128 + kPVN : t * 128 + 32; }
+  static_assert(!kP2 || 256 + 128 + kPVN + 32 <= 512, "tensor memory");
 };
 
 // MODE 1 (GEN): Nq != Nk or grouped key/value heads (fa_fwd_cross).  MODE 2 (SPARSE):
 // the butterfly block pattern (fa_fwd_sparse).  MODE 0: Nq = Nk, every query head has
 // its own key/value head, and rows always see at least one key.
-template <int D, int DT, bool CAUSAL, int MODE>
+template <int D, int DT, bool CAUSAL, int MODE, bool EARLY>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, uint16_t* __restrict__ out, float* __restrict__ lse,
@@ -132,6 +139,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // address, descriptor and loop bound derived from it) as warp-uniform
   const int warp = __shfl_sync(0xffffffffu, threadIdx.x >> 5, 0);
   const int nqb = (Nq + kTileRows - 1) / kTileRows;
+  // the next block's scores issued between the two halves of P.V (see the MMA warp):
+  // d = 64 with single-block tiles only
+  constexpr bool early_s = C::kP2 && EARLY;
   const int ntiles = forward_tiles(BH, nqb, pairing);
   // key block of step j of tile ti: j, or the j-th block of the pair's butterfly list
   auto key_block = [&](const TileInfo& ti, int j) {
@@ -148,6 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(C::kPHalf + t), kTileRows);
       mbar_init(bar(C::kPFull + t), kTileRows);
       mbar_init(bar(C::kOFull + t), 1);
+      mbar_init(bar(C::kP2Free + t), 1);
       mbar_init(bar(C::kOEmpty + t), kTileRows);
     }
     for (int i = 0; i < C::kStages; ++i) {
@@ -321,9 +332,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           // contiguous: MN-major; 16 keys = 16 rows of 128 bytes
           auto issue_pv = [&](int t, int kk0, int kk1) {
 #pragma unroll
-            for (int kk = kk0; kk < kk1; ++kk)
-              umma_ts(tmem + C::tm_o(t), tmem + C::tm_p(t) + kk * 8, vd + ((kk * 16 * 128) >> 4), idesc_pv,
+            for (int kk = kk0; kk < kk1; ++kk) {
+              // keys 0-63 read P from S_t's first columns; keys 64-127 from the next 32
+              // columns, or from tm_p2 when the next scores go in between (early_s)
+              const uint32_t pcol = (kk < 4 || !early_s) ? C::tm_p(t) + kk * 8 : C::tm_p2(t) + (kk - 4) * 8;
+              umma_ts(tmem + C::tm_o(t), tmem + pcol, vd + ((kk * 16 * 128) >> 4), idesc_pv,
                       (j > 0 || kk > 0) ? 1u : 0u);
+            }
           };
           for (int t = 0; t < 2; ++t) {
             if (j >= n[t]) continue;
@@ -335,7 +350,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc_fence_after();
-            if (elect_one()) issue_pv(t, 0, kTileRows / 32);
+            if (elect_one()) {
+              issue_pv(t, 0, kTileRows / 32);
+              // d = 64, single-block tiles: the first half's P.V was the last reader of
+              // S_t, so the next scores go now, ahead of the second half's P.V (its P has
+              // its own columns).  With pairs of blocks this shifted the two sub-tiles'
+              // exponential loops onto each other and measured 3-4 % slower.
+              if (early_s && j + 1 < n[t]) {
+                issue_s(t, qbase0 + t * C::kTileBytes, knext);
+                umma_commit(bar(C::kSFull + t));
+              }
+            }
             __syncwarp();
             if (!wait_warp(bar(C::kPFull + t), c[t] & 1, ctl, 0x207)) {
               ok = false;
@@ -344,7 +369,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             if (elect_one()) {
               issue_pv(t, kTileRows / 32, kTileRows / 16);
-              if (j + 1 < n[t]) {
+              if (early_s) {
+                // O_t now holds this block; the second-half P columns may be rewritten
+                umma_commit(bar(C::kP2Free + t));
+                if (j + 1 >= n[t]) umma_commit(bar(C::kOFull + t));
+              } else if (j + 1 < n[t]) {
                 issue_s(t, qbase0 + t * C::kTileBytes, knext);
                 umma_commit(bar(C::kSFull + t));
               } else {
@@ -376,6 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t s_addr = tmem + lane_base + C::tm_s(t);
     const uint32_t p_addr = tmem + lane_base + C::tm_p(t);
+    const uint32_t p2_addr = tmem + lane_base + C::tm_p2(t);
     const uint32_t o_addr = tmem + lane_base + C::tm_o(t);
     const uint64_t c2 = f2_pack(scale_log2, scale_log2);
     uint32_t c = 0;   // steps of this sub-tile (S-full / P-full phases)
@@ -440,9 +470,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float alpha = (GEN && m_new == m) ? 1.0f : ex2_approx(m - m_new);
         const float nm = (GEN && m_new == -INFINITY) ? 0.0f : -m_new;
         const uint64_t nm2 = f2_pack(nm, nm);
+        // d = 64: the previous block's second-half P.V may still run after this S (it
+        // was issued after it); it must be done before O is rescaled or its P columns
+        // rewritten
+        bool p2_free = !early_s || c == 0;
+        auto wait_p2 = [&]() -> bool {
+          if (p2_free) return true;
+          p2_free = __all_sync(0xffffffffu, mbar_wait(bar(C::kP2Free + t), (c - 1) & 1, ctl, 0x304));
+          return p2_free;
+        };
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
-          // O holds every earlier P.V (committed before this S); bring it to the new
-          // maximum before this block's first P.V adds to it
+          if (!wait_p2()) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // O holds every earlier P.V; bring it to the new maximum before this block's
+          // first P.V adds to it
 #pragma unroll
           for (int q = 0; q < D / 32; ++q) {
             uint32_t orr[32];
@@ -481,11 +525,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             pk[q] = pack2<DT>(p0, p1);
             if constexpr (!C::kOnesCol) accr[q & 3] = fadd2(accr[q & 3], unpack2_f2<DT>(pk[q]));
           }
-          tmem_st32(p_addr + hf * 32, pk);
+          if (hf == 1 && early_s) {
+            if (!wait_p2()) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
+          tmem_st32(hf == 0 ? p_addr : (early_s ? p2_addr : p_addr + 32), pk);
           tmem_st_wait();
           tc_fence_before();
           mbar_arrive(bar(hf == 0 ? C::kPHalf + t : C::kPFull + t));
         }
+        if (!ok) break;
         float a0, a1, b0, b1;
         f2_unpack(fadd2(acc[0], acc[1]), a0, a1);
         f2_unpack(fadd2(acc[2], acc[3]), b0, b1);
@@ -543,10 +595,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, int DT, bool CAUSAL, int MODE>
-cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
+template <int D, int DT, bool CAUSAL, int MODE, bool EARLY>
+cudaError_t launch_fwd_k(const FwdArgs& a, cudaStream_t stream, int pairing, int grid) {
   using C = FwdCfg<D>;
-  auto kern = fwd_kernel<D, DT, CAUSAL, MODE>;
+  auto kern = fwd_kernel<D, DT, CAUSAL, MODE, EARLY>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   // The register split inside the kernel must fit what the launch provides, or the
@@ -555,12 +607,22 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   e = cudaFuncGetAttributes(&attr, kern);
   if (e != cudaSuccess) return e;
   if (attr.numRegs * kThreads < (2 * kSoftmaxRegs + kOtherRegs) * 128) return cudaErrorInvalidConfiguration;
-  // (the butterfly pattern is defined on adjacent pairs of query blocks)
-  int grid = 0;
-  const int pairing = choose_pairing(a.BH, a.Nq, a.Nk, CAUSAL, MODE != 2, MODE != 2, a.num_sms, &grid);
   return launch_overlapped(kern, grid, kThreads, C::kSmemBytes, stream, a.tm_q, a.tm_k, a.tm_v,
                            static_cast<uint16_t*>(a.o), a.lse, a.BH, a.H, a.G, a.Nq, a.Nk, a.scale_log2, pairing,
                            a.err_word, a.limit_ns);
+}
+
+template <int D, int DT, bool CAUSAL, int MODE>
+cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
+  // (the butterfly pattern is defined on adjacent pairs of query blocks)
+  int grid = 0;
+  const int pairing = choose_pairing(a.BH, a.Nq, a.Nk, CAUSAL, MODE != 2, MODE != 2, a.num_sms, &grid);
+  // single-block tiles at d = 64 take the instance that issues the next scores between
+  // the two halves of P.V (+6-12 % on such launches; with pairs it measured 3-4 % slower)
+  if constexpr (D == 64 && MODE != 2) {
+    if (pairing == 2) return launch_fwd_k<D, DT, CAUSAL, MODE, true>(a, stream, pairing, grid);
+  }
+  return launch_fwd_k<D, DT, CAUSAL, MODE, false>(a, stream, pairing, grid);
 }
 
 template <int MODE>
