@@ -84,7 +84,9 @@ struct FwdCfg {
   // to spare and sums them on the CUDA cores instead.
   static constexpr bool kOnesCol = (D == 64);
   static constexpr int kOffOnes = kOffV + kStages * kTileBytes;
-  static constexpr int kOffBar = kOffOnes + (kOnesCol ? kChunkBytes : 0);
+  // split tiles: sub-tile 1's running maximum and sum per row, for sub-tile 0's merge
+  static constexpr int kOffMerge = kOffOnes + (kOnesCol ? kChunkBytes : 0);
+  static constexpr int kOffBar = kOffMerge + 2 * kTileRows * 4;
   static constexpr uint32_t kPVN = D + (kOnesCol ? 16 : 0);   // N of the P.V MMA
   // barrier indices
   static constexpr int kQFull = 0;                          // [kQBufs]
@@ -96,9 +98,10 @@ struct FwdCfg {
   static constexpr int kPHalf = kSFull + 2;                 // [2] first 64 keys of P written
   static constexpr int kPFull = kPHalf + 2;                 // [2]
   static constexpr int kOFull = kPFull + 2;                 // [2]
-  static constexpr int kP2Free = kOFull + 2;                // [2] P.V of the second 64 keys done (d = 64)
-  static constexpr int kOEmpty = kP2Free + 2;               // [2]
-  static constexpr int kDrain = kOEmpty + 2;
+  static constexpr int kOEmpty = kOFull + 2;                // [2]
+  static constexpr int kMerge = kOEmpty + 2;                // split tiles: sub-tile 1's (m, l) published
+  static constexpr int kMergeFree = kMerge + 1;             // ... and read by sub-tile 0
+  static constexpr int kDrain = kMergeFree + 1;
   static constexpr int kNumBars = kDrain + 1;
   static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;   // + alignment slack
   // tensor memory columns (512 allocated)
@@ -106,18 +109,12 @@ struct FwdCfg {
   // P_t occupies the first 64 columns of S_t; O_t (kPVN columns) follows the S buffers
   __host__ __device__ static constexpr uint32_t tm_p(int t) { return t * 128; }
   __host__ __device__ static constexpr uint32_t tm_o(int t) { return 256 + t * 128; }
-  // d = 64: P of the second 64 keys goes to 32 columns of its own after O_t's 80, so that
-  // with single-block tiles the next scores may overwrite S_t as soon as the first half's
-  // P.V has read it (d = 128 has no columns to spare: both halves of P stay in S_t)
-  static constexpr bool kP2 = (D == 64);
-  __host__ __device__ static constexpr uint32_t tm_p2(int t) { return kP2 ? 256 + t * 128 + kPVN : t * 128 + 32; }
-  static_assert(!kP2 || 256 + 128 + kPVN + 32 <= 512, "tensor memory");
 };
 
 // MODE 1 (GEN): Nq != Nk or grouped key/value heads (fa_fwd_cross).  MODE 2 (SPARSE):
 // the butterfly block pattern (fa_fwd_sparse).  MODE 0: Nq = Nk, every query head has
 // its own key/value head, and rows always see at least one key.
-template <int D, int DT, bool CAUSAL, int MODE, bool EARLY>
+template <int D, int DT, bool CAUSAL, int MODE, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, uint16_t* __restrict__ out, float* __restrict__ lse,
@@ -139,9 +136,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // address, descriptor and loop bound derived from it) as warp-uniform
   const int warp = __shfl_sync(0xffffffffu, threadIdx.x >> 5, 0);
   const int nqb = (Nq + kTileRows - 1) / kTileRows;
-  // the next block's scores issued between the two halves of P.V (see the MMA warp):
-  // d = 64 with single-block tiles only
-  constexpr bool early_s = C::kP2 && EARLY;
+  // d = 64 with single-block tiles: each tile's key blocks are split between the two
+  // sub-tiles, which merge their partial results at the end (pairing 3)
+  constexpr bool kSplit = D == 64 && SPLIT;
   const int ntiles = forward_tiles(BH, nqb, pairing);
   // key block of step j of tile ti: j, or the j-th block of the pair's butterfly list
   auto key_block = [&](const TileInfo& ti, int j) {
@@ -158,9 +155,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(C::kPHalf + t), kTileRows);
       mbar_init(bar(C::kPFull + t), kTileRows);
       mbar_init(bar(C::kOFull + t), 1);
-      mbar_init(bar(C::kP2Free + t), 1);
       mbar_init(bar(C::kOEmpty + t), kTileRows);
     }
+    mbar_init(bar(C::kMerge), kTileRows);
+    mbar_init(bar(C::kMergeFree), kTileRows);
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(bar(C::kKFull + i), 1);
       mbar_init(bar(C::kVFull + i), 1);
@@ -212,7 +210,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        const int nsub = ti.n1 > 0 ? 2 : 1;
+        const bool split = kSplit && ti.split;
+        const int nsub = split ? 1 : (ti.n1 > 0 ? 2 : 1);   // split: one query block for both
         if (elect_one()) {
           mbar_arrive_expect_tx(bar(C::kQFull + qbuf), nsub * C::kTileBytes);
           for (int t = 0; t < nsub; ++t) {
@@ -225,7 +224,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         __syncwarp();
-        for (int j = 0; j < ti.nkv; ++j, ++g) {
+        // split tiles: the loads alternate between the sub-tiles (load 2j + t is sub-tile
+        // t's j-th block; sub-tile 0 takes the last one when it has one block more)
+        const int nload = split ? ti.n0 + ti.n1 : ti.nkv;
+        for (int ld = 0; ld < nload; ++ld, ++g) {
+          const int kb = split ? key_block(ti, ld >> 1) + ((ld & 1) ? ti.koff1 : 0) : key_block(ti, ld);
           const int st = g % C::kStages;
           if (g >= (uint32_t)C::kStages &&
               !wait_warp(bar(C::kKVEmpty + st), ((g / C::kStages) - 1) & 1, ctl, 0x102)) {
@@ -238,13 +241,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(bar(C::kKFull + st), C::kTileBytes);
 #pragma unroll
             for (int c = 0; c < C::kChunks; ++c)
-              tma_load_3d(kdst + c * kChunkBytes, &tm_k, bar(C::kKFull + st), c * 64, key_block(ti, j) * kTileRows,
-                          ti.kvh);
+              tma_load_3d(kdst + c * kChunkBytes, &tm_k, bar(C::kKFull + st), c * 64, kb * kTileRows, ti.kvh);
             mbar_arrive_expect_tx(bar(C::kVFull + st), C::kTileBytes);
 #pragma unroll
             for (int c = 0; c < C::kChunks; ++c)
-              tma_load_3d(vdst + c * kChunkBytes, &tm_v, bar(C::kVFull + st), c * 64, key_block(ti, j) * kTileRows,
-                          ti.kvh);
+              tma_load_3d(vdst + c * kChunkBytes, &tm_v, bar(C::kVFull + st), c * 64, kb * kTileRows, ti.kvh);
           }
           __syncwarp();
         }
@@ -298,6 +299,74 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           continue;
         }
+        if constexpr (kSplit) {
+          // both sub-tiles multiply the tile's one Q block with their own key blocks;
+          // load 2j + t of the tile is sub-tile t's j-th key block, in a stage of its own
+          auto ld_of = [&](int t, int j) { return g + 2u * (uint32_t)j + (uint32_t)t; };
+          for (int t = 0; t < 2 && ok; ++t)
+            if (n[t] > 0 && !wait_warp(bar(C::kKFull + ld_of(t, 0) % C::kStages), (ld_of(t, 0) / C::kStages) & 1,
+                                       ctl, 0x202))
+              ok = false;
+          if (!ok) break;
+          tc_fence_after();
+          if (elect_one()) {
+            for (int t = 0; t < 2; ++t) {
+              if (n[t] == 0) continue;
+              issue_s(t, qbase0, smem_u32(smem + C::kOffK + (ld_of(t, 0) % C::kStages) * C::kTileBytes));
+              umma_commit(bar(C::kSFull + t));
+            }
+          }
+          __syncwarp();
+          for (int j = 0; ok && j < ti.nkv; ++j) {
+            for (int t = 0; t < 2; ++t) {
+              if (j >= n[t]) continue;
+              const uint32_t gj = ld_of(t, j), gn = ld_of(t, j + 1);
+              const int st = gj % C::kStages, stn = gn % C::kStages;
+              const bool more = j + 1 < n[t];
+              if ((more && !wait_warp(bar(C::kKFull + stn), (gn / C::kStages) & 1, ctl, 0x203)) ||
+                  !wait_warp(bar(C::kVFull + st), (gj / C::kStages) & 1, ctl, 0x204) ||
+                  !wait_warp(bar(C::kPHalf + t), c[t] & 1, ctl, 0x205) ||
+                  (j == 0 && e[t] > 0 && !wait_warp(bar(C::kOEmpty + t), (e[t] - 1) & 1, ctl, 0x206))) {
+                ok = false;
+                break;
+              }
+              const uint32_t vbase = smem_u32(smem + C::kOffV + st * C::kTileBytes);
+              const uint64_t vd = sdesc_sw128(vbase, smem_u32(smem + C::kOffOnes) - vbase, 1024);
+              auto issue_pv = [&](int kk0, int kk1) {
+#pragma unroll
+                for (int kk = kk0; kk < kk1; ++kk)
+                  umma_ts(tmem + C::tm_o(t), tmem + C::tm_p(t) + kk * 8, vd + ((kk * 16 * 128) >> 4), idesc_pv,
+                          (j > 0 || kk > 0) ? 1u : 0u);
+              };
+              tc_fence_after();
+              if (elect_one()) issue_pv(0, kTileRows / 32);
+              __syncwarp();
+              if (!wait_warp(bar(C::kPFull + t), c[t] & 1, ctl, 0x207)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              if (elect_one()) {
+                issue_pv(kTileRows / 32, kTileRows / 16);
+                if (more) {
+                  issue_s(t, qbase0, smem_u32(smem + C::kOffK + stn * C::kTileBytes));
+                  umma_commit(bar(C::kSFull + t));
+                } else {
+                  umma_commit(bar(C::kOFull + t));
+                }
+                umma_commit(bar(C::kKVEmpty + st));   // this stage held sub-tile t's block only
+              }
+              __syncwarp();
+              if (!more) ++e[t];
+              ++c[t];
+            }
+          }
+          if (!ok) break;
+          if (elect_one()) umma_commit(bar(C::kQEmpty + qbuf));
+          __syncwarp();
+          g += ti.n0 + ti.n1;
+          continue;
+        }
         if (!wait_warp(bar(C::kKFull + g % C::kStages), (g / C::kStages) & 1, ctl, 0x202)) break;
         tc_fence_after();
         {
@@ -332,13 +401,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           // contiguous: MN-major; 16 keys = 16 rows of 128 bytes
           auto issue_pv = [&](int t, int kk0, int kk1) {
 #pragma unroll
-            for (int kk = kk0; kk < kk1; ++kk) {
-              // keys 0-63 read P from S_t's first columns; keys 64-127 from the next 32
-              // columns, or from tm_p2 when the next scores go in between (early_s)
-              const uint32_t pcol = (kk < 4 || !early_s) ? C::tm_p(t) + kk * 8 : C::tm_p2(t) + (kk - 4) * 8;
-              umma_ts(tmem + C::tm_o(t), tmem + pcol, vd + ((kk * 16 * 128) >> 4), idesc_pv,
+            for (int kk = kk0; kk < kk1; ++kk)
+              umma_ts(tmem + C::tm_o(t), tmem + C::tm_p(t) + kk * 8, vd + ((kk * 16 * 128) >> 4), idesc_pv,
                       (j > 0 || kk > 0) ? 1u : 0u);
-            }
           };
           for (int t = 0; t < 2; ++t) {
             if (j >= n[t]) continue;
@@ -350,17 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc_fence_after();
-            if (elect_one()) {
-              issue_pv(t, 0, kTileRows / 32);
-              // d = 64, single-block tiles: the first half's P.V was the last reader of
-              // S_t, so the next scores go now, ahead of the second half's P.V (its P has
-              // its own columns).  With pairs of blocks this shifted the two sub-tiles'
-              // exponential loops onto each other and measured 3-4 % slower.
-              if (early_s && j + 1 < n[t]) {
-                issue_s(t, qbase0 + t * C::kTileBytes, knext);
-                umma_commit(bar(C::kSFull + t));
-              }
-            }
+            if (elect_one()) issue_pv(t, 0, kTileRows / 32);
             __syncwarp();
             if (!wait_warp(bar(C::kPFull + t), c[t] & 1, ctl, 0x207)) {
               ok = false;
@@ -369,11 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             if (elect_one()) {
               issue_pv(t, kTileRows / 32, kTileRows / 16);
-              if (early_s) {
-                // O_t now holds this block; the second-half P columns may be rewritten
-                umma_commit(bar(C::kP2Free + t));
-                if (j + 1 >= n[t]) umma_commit(bar(C::kOFull + t));
-              } else if (j + 1 < n[t]) {
+              if (j + 1 < n[t]) {
                 issue_s(t, qbase0 + t * C::kTileBytes, knext);
                 umma_commit(bar(C::kSFull + t));
               } else {
@@ -405,11 +456,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t s_addr = tmem + lane_base + C::tm_s(t);
     const uint32_t p_addr = tmem + lane_base + C::tm_p(t);
-    const uint32_t p2_addr = tmem + lane_base + C::tm_p2(t);
     const uint32_t o_addr = tmem + lane_base + C::tm_o(t);
     const uint64_t c2 = f2_pack(scale_log2, scale_log2);
     uint32_t c = 0;   // steps of this sub-tile (S-full / P-full phases)
     uint32_t e = 0;   // epilogues of this sub-tile
+    uint32_t mc = 0;  // split tiles merged (sub-tile 0) or published (sub-tile 1)
+    float* merge_m = reinterpret_cast<float*>(smem + C::kOffMerge);
+    float* merge_l = merge_m + kTileRows;
     for (int k = 0, tile = persistent_tile(0); tile < ntiles; tile = persistent_tile(++k)) {
       const TileInfo ti = decode_tile<MODE>(tile, BH, H, G, Nq, Nk, CAUSAL, pairing);
       const int n = t == 0 ? ti.n0 : ti.n1;
@@ -446,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
         reg_fence<128>(sr);
         float* s = reinterpret_cast<float*>(sr);
-        const int kb = key_block(ti, j);
+        const int kb = key_block(ti, j) + ((kSplit && t == 1) ? ti.koff1 : 0);
         const int kbase = kb * kTileRows;
         if (GEN ? (kbase + kTileRows - 1 > lim_blk) : ((kbase + kTileRows > Nk) || (CAUSAL && kb == qb))) {
 #pragma unroll
@@ -470,23 +523,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float alpha = (GEN && m_new == m) ? 1.0f : ex2_approx(m - m_new);
         const float nm = (GEN && m_new == -INFINITY) ? 0.0f : -m_new;
         const uint64_t nm2 = f2_pack(nm, nm);
-        // d = 64: the previous block's second-half P.V may still run after this S (it
-        // was issued after it); it must be done before O is rescaled or its P columns
-        // rewritten
-        bool p2_free = !early_s || c == 0;
-        auto wait_p2 = [&]() -> bool {
-          if (p2_free) return true;
-          p2_free = __all_sync(0xffffffffu, mbar_wait(bar(C::kP2Free + t), (c - 1) & 1, ctl, 0x304));
-          return p2_free;
-        };
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
-          if (!wait_p2()) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          // O holds every earlier P.V; bring it to the new maximum before this block's
-          // first P.V adds to it
+          // O holds every earlier P.V (committed before this S); bring it to the new
+          // maximum before this block's first P.V adds to it
 #pragma unroll
           for (int q = 0; q < D / 32; ++q) {
             uint32_t orr[32];
@@ -525,19 +564,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             pk[q] = pack2<DT>(p0, p1);
             if constexpr (!C::kOnesCol) accr[q & 3] = fadd2(accr[q & 3], unpack2_f2<DT>(pk[q]));
           }
-          if (hf == 1 && early_s) {
-            if (!wait_p2()) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-          }
-          tmem_st32(hf == 0 ? p_addr : (early_s ? p2_addr : p_addr + 32), pk);
+          tmem_st32(p_addr + hf * 32, pk);
           tmem_st_wait();
           tc_fence_before();
           mbar_arrive(bar(hf == 0 ? C::kPHalf + t : C::kPFull + t));
         }
-        if (!ok) break;
         float a0, a1, b0, b1;
         f2_unpack(fadd2(acc[0], acc[1]), a0, a1);
         f2_unpack(fadd2(acc[2], acc[3]), b0, b1);
@@ -555,12 +586,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kOFull + t), e & 1, ctl, 0x303))) break;
       ++e;
       tc_fence_after();
+      if constexpr (kSplit) {
+        if (t == 1) {
+          // split tile: hand this half's running maximum and sum to sub-tile 0, which
+          // merges the two halves (it reads O_1 from tensor memory: the same rows) and
+          // frees both O buffers
+          if (!__all_sync(0xffffffffu, mc == 0 || mbar_wait(bar(C::kMergeFree), (mc - 1) & 1, ctl, 0x305))) break;
+          merge_m[tid] = m;
+          merge_l[tid] = l;
+          ++mc;
+          mbar_arrive(bar(C::kMerge));
+          continue;
+        }
+      }
       if constexpr (C::kOnesCol) {   // the MMA summed the 16-bit P values into O column D
         uint32_t orr[16];
         tmem_ld16(o_addr + D, orr);
         tmem_ld_wait();
         reg_fence<16>(orr);
         lr = __uint_as_float(orr[0]);
+      }
+      // split tile: m = max(m_0, m_1), O = (O_0 2^(m_0 - m) + O_1 2^(m_1 - m)) / (lr_0 2^(m_0 - m)
+      // + lr_1 2^(m_1 - m)) and l likewise: the merge of two blocks' statistics
+      const bool merge = kSplit && ti.n1 > 0;
+      const uint32_t o1_addr = tmem + lane_base + C::tm_o(1);
+      float a0 = 1.0f, a1 = 0.0f;
+      if (merge) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(C::kMerge), mc & 1, ctl, 0x306))) break;
+        tc_fence_after();   // O_1 is complete: sub-tile 1 saw its last P.V before publishing
+        ++mc;
+        const float m1 = merge_m[tid], l1 = merge_l[tid];
+        mbar_arrive(bar(C::kMergeFree));
+        uint32_t orr[16];
+        tmem_ld16(o1_addr + D, orr);   // sub-tile 1's sum of the 16-bit P values
+        tmem_ld_wait();
+        reg_fence<16>(orr);
+        const float lr1 = __uint_as_float(orr[0]);
+        const float mm = fmaxf(m, m1);
+        a0 = m == -INFINITY ? 0.0f : ex2_approx(m - mm);
+        a1 = m1 == -INFINITY ? 0.0f : ex2_approx(m1 - mm);
+        l = l * a0 + l1 * a1;
+        lr = lr * a0 + lr1 * a1;
+        m = mm;
       }
       const float inv_l = (!GEN || lr > 0.0f) ? 1.0f / lr : 0.0f;   // a row that saw no key: O = 0
       uint8_t* orow = reinterpret_cast<uint8_t*>(out) + ((size_t)ti.bh * Nq + row) * (D * 2);
@@ -570,6 +637,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(o_addr + q * 32, orr);
         tmem_ld_wait();
         reg_fence<32>(orr);
+        if (merge) {
+          uint32_t o1[32];
+          tmem_ld32(o1_addr + q * 32, o1);
+          tmem_ld_wait();
+          reg_fence<32>(o1);
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            orr[i] = __float_as_uint(fmaf(__uint_as_float(orr[i]), a0, __uint_as_float(o1[i]) * a1));
+        }
         uint32_t w[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
@@ -583,6 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (row < Nq) lse[(size_t)ti.bh * Nq + row] = (m + lg2_approx(l)) * 0.69314718055994530942f;
       tc_fence_before();
       mbar_arrive(bar(C::kOEmpty + t));
+      if (merge) mbar_arrive(bar(C::kOEmpty + 1));
     }
   }
 
@@ -595,10 +672,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, int DT, bool CAUSAL, int MODE, bool EARLY>
+template <int D, int DT, bool CAUSAL, int MODE, bool SPLIT>
 cudaError_t launch_fwd_k(const FwdArgs& a, cudaStream_t stream, int pairing, int grid) {
   using C = FwdCfg<D>;
-  auto kern = fwd_kernel<D, DT, CAUSAL, MODE, EARLY>;
+  auto kern = fwd_kernel<D, DT, CAUSAL, MODE, SPLIT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   // The register split inside the kernel must fit what the launch provides, or the
@@ -617,10 +694,10 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   // (the butterfly pattern is defined on adjacent pairs of query blocks)
   int grid = 0;
   const int pairing = choose_pairing(a.BH, a.Nq, a.Nk, CAUSAL, MODE != 2, MODE != 2, a.num_sms, &grid);
-  // single-block tiles at d = 64 take the instance that issues the next scores between
-  // the two halves of P.V (+6-12 % on such launches; with pairs it measured 3-4 % slower)
+  // single-block tiles at d = 64: the instance that splits each tile's key blocks between
+  // the two sub-tiles (pairing 3), so that both softmax warpgroups work
   if constexpr (D == 64 && MODE != 2) {
-    if (pairing == 2) return launch_fwd_k<D, DT, CAUSAL, MODE, true>(a, stream, pairing, grid);
+    if (pairing == 2) return launch_fwd_k<D, DT, CAUSAL, MODE, true>(a, stream, 3, grid);
   }
   return launch_fwd_k<D, DT, CAUSAL, MODE, false>(a, stream, pairing, grid);
 }

@@ -23,6 +23,8 @@ constexpr int kTileRows = 128;   // query rows per sub-tile and keys per key/val
 struct TileInfo {
   int bh, kvh, qb0, qb1, n0, n1, nkv;
   bool has1;   // the second query block exists (it may still see no key)
+  bool split;  // pairing 3: both sub-tiles take query block qb0, sub-tile 1 from key block koff1
+  int koff1;
 };
 
 // Key/value blocks visible to query block qb: all of them without the causal mask;
@@ -48,6 +50,9 @@ __host__ __device__ __forceinline__ int visible_kv_blocks(int qb, int Nq, int Nk
 //   2 single    one query block per tile, heaviest first: for launches with fewer pairs
 //               than SMs, so that every SM works and a lone softmax warpgroup runs
 //               without the other's contention.
+//   3 split     single query blocks as in 2, with the block's keys cut in two: sub-tile 0
+//               takes the first ceil(n/2) key blocks, sub-tile 1 the rest (koff1 on), and
+//               the two partial results are merged at the end (16-bit forward, d = 64).
 // MODE: 0 plain (Nq = Nk, one key/value head per query head), 1 general (fa_fwd_cross),
 // 2 butterfly block pattern (fa_fwd_sparse).
 template <int MODE>
@@ -59,7 +64,7 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, int BH, int H, int G, 
   const int r = tile / BH;
   ti.bh = tile - r * BH;
   ti.kvh = MODE == 1 ? (ti.bh / H) * (H / G) + (ti.bh % H) / G : ti.bh;
-  if (pairing == 2) {
+  if (pairing >= 2) {
     ti.qb0 = nqb - 1 - r;
     ti.qb1 = nqb;   // none
   } else if (pairing == 1) {
@@ -83,6 +88,16 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, int BH, int H, int G, 
     ti.n0 = causal ? ti.qb0 + 1 : nqb;
     ti.n1 = ti.has1 ? (causal ? ti.qb1 + 1 : nqb) : 0;
   }
+  ti.split = false;
+  ti.koff1 = 0;
+  if (pairing == 3) {
+    const int n = ti.n0;
+    ti.n0 = (n + 1) >> 1;
+    ti.n1 = n - ti.n0;
+    ti.qb1 = ti.qb0;
+    ti.koff1 = ti.n0;
+    ti.split = true;
+  }
   ti.nkv = ti.n0 > ti.n1 ? ti.n0 : ti.n1;
   return ti;
 }
@@ -93,7 +108,7 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, int BH, int H, int G, 
 // so the simulation is only run for small launches.
 // Tiles of a launch with this pairing.
 __host__ __device__ __forceinline__ int forward_tiles(int BH, int nqb, int pairing) {
-  return BH * (pairing == 2 ? nqb : (nqb + 1) >> 1);
+  return BH * (pairing >= 2 ? nqb : (nqb + 1) >> 1);
 }
 
 // Pairing of a launch: single query blocks when there are fewer pairs than SMs (and the

@@ -53,10 +53,17 @@ def test_butterfly_matches_oracle(B, H, N, d, dtype, causal):
 
 
 def test_single_pair_is_dense():
-    """With at most 256 keys the pattern is one block: bitwise the dense kernels."""
+    """With at most 256 keys the pattern is one block: the sparse and the dense kernels
+    both give the dense causal result.  (They need not agree bit for bit: a launch this
+    small runs the dense forward with each query block's keys split between the two
+    sub-tiles and merged.)"""
     c = make_case(1, 4, 250, 64, "bf16", True, workload_index=221)
     q, k, v = (G.to_device(getattr(c, n), "bf16") for n in ("q", "k", "v"))
     o1, l1 = forward(q, k, v, causal=True, pattern="butterfly")
     o2, l2 = forward(q, k, v, causal=True)
     torch.cuda.synchronize()
-    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    for h in range(4):
+        f = lambda name: bits_to_f64(getattr(c, name)[0, h], "bf16")  # noqa: E731
+        o_ref, lse_ref = oracle.attn_head_fwd(f("q"), f("k"), f("v"), c.scale, True)
+        for o, lse, label in ((o1, l1, "butterfly"), (o2, l2, "dense")):
+            G.check_forward(G.to_f64(o[0, h]), G.to_f64(lse[0, h]), o_ref, lse_ref, f"{label} N250 head {h}", "bf16")
