@@ -54,10 +54,18 @@ constexpr int kRows = 128;
 constexpr int kChunkBytes = kRows * 128;
 constexpr int kBwdThreads = 512;
 constexpr int kBwdLaunchRegs = 128;
+// Register split (setmaxnreg) per warpgroup: the two dS warpgroups, the dQ warpgroup and
+// the control warps (producer, MMA issuer).  At d = 128 the dQ warpgroup gets 112 (its
+// 64 columns of dQ per staging round and the dK/dV read-out spilled at 96) and the control
+// warps 80: +7.6 % on the d = 128 backward.  At d = 64 the same split measured 2 % slower,
+// so it keeps 96 / 96.
 constexpr int kDsRegs = 160;
-constexpr int kDqRegs = 96;
-constexpr int kCtlRegs = 96;
-static_assert((2 * kDsRegs + kDqRegs + kCtlRegs) * 128 <= kBwdLaunchRegs * kBwdThreads,
+template <int D>
+constexpr int kDqRegs = D == 128 ? 112 : 96;
+template <int D>
+constexpr int kCtlRegs = D == 128 ? 80 : 96;
+static_assert((2 * kDsRegs + kDqRegs<64> + kCtlRegs<64>) * 128 <= kBwdLaunchRegs * kBwdThreads &&
+                  (2 * kDsRegs + kDqRegs<128> + kCtlRegs<128>) * 128 <= kBwdLaunchRegs * kBwdThreads,
               "register split exceeds the launch");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kTileSlots = 4;   // tile numbers the producer may publish ahead of the slowest role
@@ -233,7 +241,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   };
 
   if (warp >= 12) {
-    regs_dec<kCtlRegs>();
+    regs_dec<kCtlRegs<D>>();
     if (warp == 12) {
       // ---------------------------------------------------------- TMA producer (whole warp; one lane issues)
       if (elect_one()) {
@@ -575,7 +583,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ dQ warpgroup: dQ reduction, dK/dV epilogue
-    regs_dec<kDqRegs>();
+    regs_dec<kDqRegs<D>>();
     const int u = threadIdx.x - 256;
     const int dq_warp = warp - 8;          // rows 32*dq_warp .. +31 of each query block
     const int lane = threadIdx.x & 31;
@@ -790,7 +798,7 @@ cudaError_t launch_kv_t(const BwdArgs& a, cudaStream_t stream) {
   cudaFuncAttributes attr;
   e = cudaFuncGetAttributes(&attr, kern);
   if (e != cudaSuccess) return e;
-  if (attr.numRegs * kBwdThreads < (2 * kDsRegs + kDqRegs + kCtlRegs) * 128) return cudaErrorInvalidConfiguration;
+  if (attr.numRegs * kBwdThreads < (2 * kDsRegs + kDqRegs<D> + kCtlRegs<D>) * 128) return cudaErrorInvalidConfiguration;
   const int nb = (a.N + kRows - 1) / kRows;
   const int ntiles = a.BHkv * nb;
   const int grid = ntiles < a.num_sms ? ntiles : a.num_sms;
