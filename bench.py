@@ -304,6 +304,10 @@ def run_ours(args, w, rank, world, local_rank):
         for it in range(total):
             b = it % 2
             if it == 2:
+                # the two untimed steps fill both buffer sets; the timed window opens on an
+                # idle GPU with step 2's upload, so it holds exactly e2e_steps uploads,
+                # computes and read-backs (overlapped with one another) and nothing else
+                torch.cuda.synchronize()
                 e0.record(s_in)
             with torch.cuda.stream(s_in):          # upload step it (after step it-2 used the buffer)
                 s_in.wait_event(ev_comp[b])
