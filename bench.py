@@ -209,16 +209,21 @@ def run_ours(args, w, rank, world, local_rank):
     n_ev = 2 + len(stages)
     launches_per_step = 1 + len(stages)
 
-    def step(evs=None):
+    def step(evs=None, per_launch=True):
+        # per_launch: an event after every launch (the launches then run one after
+        # another); otherwise events at the step's two ends only, so that each launch's
+        # set-up overlaps the previous kernel's tail as it does in a training loop
         if evs:
             evs[0].record(stream)
         fwd()
-        if evs:
+        if evs and per_launch:
             evs[1].record(stream)
         for i, fn in enumerate(stages):
             call(fn(*bwd_args()), fn.__name__)
-            if evs:
+            if evs and per_launch:
                 evs[2 + i].record(stream)
+        if evs and not per_launch:
+            evs[1].record(stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -227,7 +232,11 @@ def run_ours(args, w, rank, world, local_rank):
     if fa.last_kernel_status() != 0:
         raise RuntimeError("a kernel reported a pipeline timeout during warm-up")
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+    # The timed steps alternate: even steps are bracketed by two events (the step time),
+    # odd steps carry an event after every launch (the per-kernel times of the roofline).
+    # A forward-only step has one launch, so every step serves both.
+    per_launch = [not stages or i % 2 == 1 or args.steps == 1 for i in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev if pl else 2)] for pl in per_launch]
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -240,7 +249,7 @@ def run_ours(args, w, rank, world, local_rank):
     wall0 = time.perf_counter()
     for i in range(args.steps):
         flush.zero_()
-        step(ev[i])
+        step(ev[i], per_launch[i])
     torch.cuda.synchronize()
     wall1 = time.perf_counter()
     if world > 1:
@@ -250,12 +259,17 @@ def run_ours(args, w, rank, world, local_rank):
     if status != 0:
         raise RuntimeError(f"a kernel reported {fa.STATUS.get(status)} in the timed region")
 
-    # median over the timed steps of each launch's event time
-    seg = [[ev[i][j].elapsed_time(ev[i][j + 1]) for j in range(n_ev - 1)] for i in range(args.steps)]
+    # medians over the timed steps: each launch's event time (steps with per-launch
+    # events) and the whole step (steps bracketed at their ends only)
+    seg = [[ev[i][j].elapsed_time(ev[i][j + 1]) for j in range(n_ev - 1)]
+           for i in range(args.steps) if per_launch[i]]
     t_fwd = statistics.median(s[0] for s in seg)
     t_stage = [statistics.median(s[1 + j] for s in seg) for j in range(len(stages))]
     t_bwd = sum(t_stage)
-    t_step = t_fwd + t_bwd
+    whole = [ev[i][0].elapsed_time(ev[i][-1]) for i in range(args.steps) if not per_launch[i] or not stages]
+    t_serial = t_fwd + t_bwd
+    t_step = statistics.median(whole) if whole else t_serial
+    n_whole, n_per = len(whole), len(seg)
     if world > 1:
         t_step, t_fwd, t_bwd = reduce_step_times([t_step, t_fwd, t_bwd], device=dev)
 
@@ -364,7 +378,11 @@ def run_ours(args, w, rank, world, local_rank):
                         "fwd_bwd": round(100 * f_step / (t_step * 1e-3) / 1e12 / peak_burst, 2),
                         "peak": f"{peak_burst} TFLOP/s dense bf16 ({peak_src}, burst)"},
         "ms": {"fwd": round(t_fwd, 5), "bwd": round(t_bwd, 5),
-               "bwd_stages": [round(x, 5) for x in t_stage]},
+               "bwd_stages": [round(x, 5) for x in t_stage], "launches_one_by_one": round(t_serial, 5)},
+        "timing": (f"ms_per_step: median of {n_whole} timed steps with events at their two ends only; "
+                   f"ms, tflops.fwd/bwd and roofline: medians of {n_per} timed steps with an event after "
+                   "every launch, which serialises the launches" if stages else
+                   f"median of {n_whole} timed steps, one launch each"),
         "roofline": roofline,
         "gpu_launches": launches_per_step * args.steps,
         "wall_s_timed": round(wall1 - wall0, 3),
