@@ -75,6 +75,13 @@ def reduce_step_times(times, device=None):
     return [float(x) for x in t.tolist()]
 
 
+def step_brackets(steps, launches):
+    """Event bracketing of the timed steps: True for a step with an event after every
+    launch (the per-kernel times), False for one with events at its two ends only (the
+    step time).  The two alternate; a one-launch step, or a single timed step, serves both."""
+    return [launches == 1 or steps == 1 or i % 2 == 1 for i in range(steps)]
+
+
 def job_throughput(world, flops_per_step, ms_per_step):
     """Whole-job TFLOP/s of `world` replicas that each do `flops_per_step` per step and
     take (at most, over ranks) `ms_per_step`."""
@@ -235,7 +242,7 @@ def run_ours(args, w, rank, world, local_rank):
     # The timed steps alternate: even steps are bracketed by two events (the step time),
     # odd steps carry an event after every launch (the per-kernel times of the roofline).
     # A forward-only step has one launch, so every step serves both.
-    per_launch = [not stages or i % 2 == 1 or args.steps == 1 for i in range(args.steps)]
+    per_launch = step_brackets(args.steps, launches_per_step)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev if pl else 2)] for pl in per_launch]
     dist = None
     if world > 1:

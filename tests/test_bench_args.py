@@ -32,3 +32,12 @@ def test_oracle_sample_is_bounded_and_counts_work():
     n, rows, el, tf = bench.oracle_sample(w, 0.0, max_samples=2)
     assert n == 1 and rows == w["N"] and el > 0 and tf > 0
     assert "whole (b,h) heads" in bench.sample_text(w, n, rows, el)
+
+
+def test_step_brackets_alternate_whole_steps_and_per_launch_steps():
+    plan = bench.step_brackets(20, 4)
+    assert plan.count(True) == 10 and plan.count(False) == 10
+    assert plan[0] is False and plan[1] is True
+    assert bench.step_brackets(1, 4) == [True]                    # one step: per-launch times and the step
+    assert bench.step_brackets(5, 1) == [True] * 5                # a forward-only step is one launch
+    assert bench.step_brackets(3, 4) == [False, True, False]
