@@ -389,7 +389,9 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
   BwdArgs a;
   const int BH = B * H;
   if (!encode_bhnd(&a.tm_q, q, BH, N, d, dtype) || !encode_bhnd(&a.tm_k, k, B * Hkv, N, d, dtype) ||
-      !encode_bhnd(&a.tm_v, v, B * Hkv, N, d, dtype) || !encode_bhnd(&a.tm_do, dO, BH, N, d, dtype))
+      !encode_bhnd(&a.tm_v, v, B * Hkv, N, d, dtype) || !encode_bhnd(&a.tm_do, dO, BH, N, d, dtype) ||
+      !encode_bhnd_rows(&a.tm_dk, dk, B * Hkv, N, d, dtype, 32) ||
+      !encode_bhnd_rows(&a.tm_dv, dv, B * Hkv, N, d, dtype, 32))
     return FA_ERR_LAUNCH;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.o = o;

@@ -34,7 +34,8 @@
 //                    shared-memory tile that one thread adds into the float32
 //                    accumulator with a bulk tensor reduction (whole 128-byte
 //                    lines, done by the copy engine); writes dK and dV at the end
-//                    of a tile
+//                    of a tile (on short d = 64 tiles staged in the same ring and
+//                    written by bulk tensor stores)
 //   warp 12          TMA producer; warp 13 MMA issuer; warps 14-15 idle
 //
 // At d = 64 the tensor-memory columns hold S^T, dP^T, dV, dK, dQ and P^T side by side,
@@ -67,7 +68,6 @@ constexpr int kCtlRegs = D == 128 ? 80 : 96;
 static_assert((2 * kDsRegs + kDqRegs<64> + kCtlRegs<64>) * 128 <= kBwdLaunchRegs * kBwdThreads &&
                   (2 * kDsRegs + kDqRegs<128> + kCtlRegs<128>) * 128 <= kBwdLaunchRegs * kBwdThreads,
               "register split exceeds the launch");
-constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kTileSlots = 4;   // tile numbers the producer may publish ahead of the slowest role
 
 template <int D, bool WIDE = false>
@@ -143,12 +143,16 @@ template <int D, int DT, bool CAUSAL, int MODE, bool WIDE>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                  const __grid_constant__ CUtensorMap tm_dq, const uint8_t* __restrict__ stats, float* __restrict__ dq_accum,
+                  const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
+                  const __grid_constant__ CUtensorMap tm_dv, const uint8_t* __restrict__ stats, float* __restrict__ dq_accum,
                   unsigned int* __restrict__ tile_counter,
                   uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, int BHkv, int H, int G, int N, int Npad,
                   float scale,
                   float scale_log2, int hg, unsigned int* err_word, uint64_t limit_ns) {
   using C = BwdCfg<D, WIDE>;
+  // dK/dV written through the dQ staging ring by bulk tensor stores on short tiles at d = 64
+  // (the tile-end read-out is then off the dQ warpgroup's load/store pipe)
+  constexpr bool kStagedDKV = D == 64 && !WIDE;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned base, derived from the __shared__ array by pointer arithmetic so
   // that every access through it stays a shared-memory access (not a generic one)
@@ -590,8 +594,59 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint32_t dq_chunks = 0;                // chunks this warp has staged (its ring position)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     // dK (times scale) and dV of the key block, read out of tensor memory; the columns
-    // are handed back to the MMA warp as soon as the last of them is in registers
-    auto write_dkdv = [&](int it, int kb, int bh) -> bool {
+    // are handed back to the MMA warp as soon as the last of them is in registers.  Each
+    // warp stages its 32 rows as 16-bit values in its own dQ staging ring (4 KB per 64
+    // columns, 128-byte swizzle: conflict-free) and writes them with bulk tensor stores,
+    // instead of one 16-byte global store per row and unit (32 lines per instruction)
+    bool dkdv_staged = false;   // the ring holds dK/dV rows that a store may still be reading
+    auto write_dkdv_staged = [&](int it, int kb, int bh) -> bool {
+      if (!wait_warp(bar(C::kDKVFull), it & 1, ctl, 0x702)) return false;
+      tc_fence_after();
+      uint8_t* ring = smem + C::kOffDQS + dq_warp * C::kDQRing * C::kDQChunkBytes;
+      const int row0 = kb * kRows + 32 * dq_warp;   // rows past N are not written by the store
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col0 = which == 0 ? C::kTmDV : C::kTmDK;
+        const float mul = which == 0 ? 1.0f : scale;
+        // every earlier bulk operation of this warp (dQ reductions, the dV store) has read the ring
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_base + col0 + c * 32, r);
+          tmem_ld_wait();
+          reg_fence<32>(r);
+          if (which == 1 && c == D / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(bar(C::kDKVEmpty));
+          }
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack2<DT>(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
+          // 32 columns are 4 of the 8 16-byte units of this lane's 128-byte row in block c / 2
+          uint8_t* row = ring + (c >> 1) * 4096 + lane * 128;
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            *reinterpret_cast<uint4*>(row + ((((c & 1) * 4 + v) ^ (lane & 7)) << 4)) =
+                make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+          for (int c2 = 0; c2 < D / 64; ++c2)
+            tma_store_3d(which == 0 ? &tm_dv : &tm_dk, smem_u32(ring) + c2 * 4096, c2 * 64, row0, bh);
+          bulk_commit_group();
+        }
+      }
+      dkdv_staged = true;
+      return true;
+    };
+    // (long tiles and d = 128: one 16-byte global store per row and unit, measured
+    // faster there than the staged form above)
+    auto write_dkdv_rows = [&](int it, int kb, int bh) -> bool {
       if (!wait_warp(bar(C::kDKVFull), it & 1, ctl, 0x702)) return false;
       tc_fence_after();
       const int key = kb * kRows + u;
@@ -622,6 +677,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
       return true;
+    };
+    auto write_dkdv = [&](int it, int kb, int bh) -> bool {
+      if constexpr (kStagedDKV) return write_dkdv_staged(it, kb, bh);
+      else return write_dkdv_rows(it, kb, bh);
     };
     uint32_t s = 0;
     int it = 0;
@@ -663,9 +722,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int q = 0; q < 64 / C::kDQCols; ++q) {   // chunks of kDQCols columns
             uint8_t* box = smem + C::kOffDQS + (dq_warp * C::kDQRing + dq_chunks % C::kDQRing) * C::kDQChunkBytes;
-            // the reduction that last read this buffer must be done reading it
-            if (lane == 0 && dq_chunks >= (uint32_t)C::kDQRing) bulk_wait_read<C::kDQRing - 1>();
+            // the reduction that last read this buffer must be done reading it (after a
+            // dK/dV write-out: the stores, which read the whole ring)
+            if (lane == 0) {
+              if (dkdv_staged) bulk_wait_read<0>();
+              else if (dq_chunks >= (uint32_t)C::kDQRing) bulk_wait_read<C::kDQRing - 1>();
+            }
             __syncwarp();
+            dkdv_staged = false;
             if constexpr (WIDE) {
               const uint32_t* src = r[q];
 #pragma unroll
@@ -803,7 +867,7 @@ cudaError_t launch_kv_t(const BwdArgs& a, cudaStream_t stream) {
   const int ntiles = a.BHkv * nb;
   const int grid = ntiles < a.num_sms ? ntiles : a.num_sms;
   return launch_overlapped(kern, grid, kBwdThreads, C::kSmemBytes, stream, a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dq,
-                           a.stats, a.dq_accum, a.tile_counter, static_cast<uint16_t*>(a.dk),
+                           a.tm_dk, a.tm_dv, a.stats, a.dq_accum, a.tile_counter, static_cast<uint16_t*>(a.dk),
                            static_cast<uint16_t*>(a.dv), a.BHkv, a.H, a.G, a.N, a.Npad, a.scale, a.scale_log2,
                            a.heads_per_group, a.err_word, a.limit_ns);
 }

@@ -30,6 +30,7 @@ struct FwdArgs {
 struct BwdArgs {
   CUtensorMap tm_q, tm_do;       // {d, N, B*H}
   CUtensorMap tm_k, tm_v;        // {d, N, B*Hkv}
+  CUtensorMap tm_dk, tm_dv;      // {d, N, B*Hkv}, box {64, 32, 1}, 128-byte swizzle: the dK/dV stores
   CUtensorMap tm_dq;  // 3-D map {d, N, B*H} over the float32 dQ accumulator, box {16, 32, 1}
                       // (64-byte swizzle), or {32, 32, 1} (128-byte swizzle) when wide_dq
   const void* o;
