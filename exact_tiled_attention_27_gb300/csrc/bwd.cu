@@ -153,6 +153,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // dK/dV written through the dQ staging ring by bulk tensor stores on short tiles at d = 64
   // (the tile-end read-out is then off the dQ warpgroup's load/store pipe)
   constexpr bool kStagedDKV = D == 64 && !WIDE;
+  // short d = 64 tiles: the next tile is claimed a tile ahead and its first scores are
+  // issued during the current tile's last step when its operands are already in place
+  constexpr bool kAhead = C::kKVBufs == 2 && !WIDE;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned base, derived from the __shared__ array by pointer arithmetic so
   // that every access through it stays a shared-memory access (not a generic one)
@@ -257,6 +260,107 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint32_t s = 0;
       int it = 0;
       bool ok = true;
+      if constexpr (kAhead) {
+        // short d = 64 tiles: the tile after the current one is claimed as soon as the current
+        // one starts, and its K and V go into the other buffer as soon as that buffer is free
+        // (checked between this tile's Q/dO loads, waited for at its end), so that the MMA warp
+        // can issue the next tile's first scores during this tile's last step
+        auto publish = [&](int k, int tile) -> bool {
+          const int slot = k % kTileSlots;
+          if (k >= kTileSlots && !wait_warp(bar(C::kTileEmpty + slot), ((k / kTileSlots) - 1) & 1, ctl, 0x403))
+            return false;
+          if ((threadIdx.x & 31) == 0) {
+            tile_ring[slot] = tile;
+            mbar_arrive(bar(C::kTileFull + slot));   // release: the ring entry is visible with the phase
+          }
+          __syncwarp();
+          return true;
+        };
+        auto issue_kv = [&](int k, int tile) {      // K and V of tile number k into buffer k % 2
+          int kb, bh;
+          group_order(tile, BHkv, nb, hg, kb, bh);
+          const int kvb = k % C::kKVBufs;
+          const uint32_t kdst = smem_u32(smem + C::kOffK + kvb * C::kTileBytes);
+          const uint32_t vdst = smem_u32(smem + C::kOffV + kvb * C::kTileBytes);
+          if (elect_one()) {
+            mbar_arrive_expect_tx(bar(C::kKVFull + kvb), 2 * C::kTileBytes);
+#pragma unroll
+            for (int c = 0; c < C::kChunks; ++c) {
+              tma_load_3d(kdst + c * kChunkBytes, &tm_k, bar(C::kKVFull + kvb), c * 64, kb * kRows, bh);
+              tma_load_3d(vdst + c * kChunkBytes, &tm_v, bar(C::kKVFull + kvb), c * 64, kb * kRows, bh);
+            }
+          }
+          __syncwarp();
+        };
+        // buffer of tile number k free (the tile two earlier done with it); without blocking
+        // unless `block`: 1 free, 0 not yet, -1 the wait gave up
+        auto kv_free = [&](int k, bool block) -> int {
+          if (k < C::kKVBufs) return 1;
+          const uint32_t eb = bar(C::kKVEmpty + k % C::kKVBufs), par = ((k / C::kKVBufs) - 1) & 1;
+          if (block) return wait_warp(eb, par, ctl, 0x401) ? 1 : -1;
+          return __all_sync(0xffffffffu, mbar_test(eb, par) != 0u) ? 1 : 0;
+        };
+        int kv_done = 0;   // tile numbers whose K and V were issued
+        int cur = static_cast<int>(blockIdx.x) < ntiles ? static_cast<int>(blockIdx.x) : -1;
+        ok = publish(0, cur);
+        if (ok && cur >= 0) {
+          issue_kv(0, cur);
+          kv_done = 1;
+        }
+        for (; ok && cur >= 0; ++it) {
+          unsigned int claim = 0;
+          if ((threadIdx.x & 31) == 0) claim = atomicAdd(tile_counter, 1u);
+          int nxt = static_cast<int>(gridDim.x + __shfl_sync(0xffffffffu, claim, 0));
+          if (nxt >= ntiles) nxt = -1;
+          if (!publish(it + 1, nxt)) {
+            ok = false;
+            break;
+          }
+          int kb, bh;
+          group_order(cur, BHkv, nb, hg, kb, bh);
+          const int q0 = SPARSE ? sparse_q(kb, 0) : (CAUSAL ? kb : 0);
+          const int nq = SPARSE ? sparse_n(kb) : 0;
+          for (int g = 0; ok && g < group; ++g) {
+          const int bhq = first_q_head(bh) + g;
+          for (int qi = q0, j = 0; SPARSE ? j < nq : qi < nb; ++s, ++j, qi = SPARSE ? sparse_q(kb, j) : qi + 1) {
+            if (nxt >= 0 && kv_done == it + 1 && kv_free(it + 1, false) == 1) {
+              issue_kv(it + 1, nxt);
+              kv_done = it + 2;
+            }
+            const int qs = s % C::kQBufs;
+            if (s >= (uint32_t)C::kQBufs && !wait_warp(bar(C::kQEmpty + qs), ((s / C::kQBufs) - 1) & 1, ctl, 0x402)) {
+              ok = false;
+              break;
+            }
+            const uint32_t qdst = smem_u32(smem + C::kOffQ + qs * C::kTileBytes);
+            const uint32_t odst = smem_u32(smem + C::kOffDO + qs * C::kTileBytes);
+            const uint32_t sdst = smem_u32(smem + C::kOffStats + qs * kStatsTileBytes);
+            if (elect_one()) {
+              mbar_arrive_expect_tx(bar(C::kQFull + qs), 2 * C::kTileBytes + kStatsTileBytes);
+#pragma unroll
+              for (int c = 0; c < C::kChunks; ++c) {
+                tma_load_3d(qdst + c * kChunkBytes, &tm_q, bar(C::kQFull + qs), c * 64, qi * kRows, bhq);
+                tma_load_3d(odst + c * kChunkBytes, &tm_do, bar(C::kQFull + qs), c * 64, qi * kRows, bhq);
+              }
+              const size_t sblock = (size_t)bhq * (Npad / kRows) + qi;
+              bulk_load(sdst, stats + sblock * kStatsTileBytes, kStatsTileBytes, bar(C::kQFull + qs));
+            }
+            __syncwarp();
+          }
+          }
+          if (!ok) break;
+          if (nxt >= 0 && kv_done == it + 1) {
+            if (kv_free(it + 1, true) != 1) {
+              ok = false;
+              break;
+            }
+            issue_kv(it + 1, nxt);
+            kv_done = it + 2;
+          }
+          cur = nxt;
+        }
+        it = kv_done;   // the drain below waits for every K/V load issued
+      } else {
       int next = static_cast<int>(blockIdx.x);
       for (;; ++it) {
         const int slot = it % kTileSlots;
@@ -326,6 +430,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if ((threadIdx.x & 31) == 0) claim = atomicAdd(tile_counter, 1u);
         next = static_cast<int>(gridDim.x + __shfl_sync(0xffffffffu, claim, 0));
       }
+      }
       if (!ok) {
         // let every copy already issued land before the CTA exits
         for (int b = 0; b < C::kKVBufs; ++b)
@@ -376,138 +481,314 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       };
       auto issue_fold_s = [&](uint32_t step) { umma_ss(tmem + C::kTmST, a_lse, stats_desc(step), idesc_s, 1u); };
       auto issue_fold_dp = [&](uint32_t step) { umma_ss(tmem + C::kTmDPT, a_d, stats_desc(step), idesc_s, 1u); };
-      uint32_t s = 0;
-      int it = 0;
-      bool ok = true;
-      for (;; ++it) {
-        const int tile = take_tile(it, 0x50f);
-        if (tile < 0) break;
-        int kb, bh;
-        group_order(tile, BHkv, nb, hg, kb, bh);
-        const int kvb = it % C::kKVBufs;
-        const int q0 = CAUSAL ? kb : 0;
-        const int nsteps = SPARSE ? sparse_n(kb) : group * (nb - q0);
-        if (!wait_warp(bar(C::kKVFull + kvb), (it / C::kKVBufs) & 1, ctl, 0x501)) break;
-        const uint32_t kbase = smem_u32(smem + C::kOffK + kvb * C::kTileBytes);
-        const uint32_t vbase = smem_u32(smem + C::kOffV + kvb * C::kTileBytes);
-        // first block of the tile
-        if (!wait_warp(bar(C::kQFull + s % C::kQBufs), (s / C::kQBufs) & 1, ctl, 0x502) ||
-            (s > 0 && !wait_warp(bar(C::kSTFree), (s - 1) & 1, ctl, 0x503)) ||
-            (!C::kEarly && s > 0 && !wait_warp(bar(C::kDQFree), (s - 1) & 1, ctl, 0x504))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (elect_one()) {
-          issue_st(kbase, qaddr(s));
-          issue_fold_s(s);
-          issue_dpt(vbase, oaddr(s));
-          issue_fold_dp(s);
-          umma_commit(bar(C::kSFull));
-        }
-        __syncwarp();
-        for (int i = 0; i < nsteps; ++i, ++s) {
-          const bool last = (i == nsteps - 1);
-          if (C::kEarly && !last) {
-            if (!wait_warp(bar(C::kQFull + (s + 1) % C::kQBufs), ((s + 1) / C::kQBufs) & 1, ctl, 0x505) ||
-                !wait_warp(bar(C::kSTFree), s & 1, ctl, 0x506)) {
+      // Short d = 64 tiles take the next tile during the last step and may issue its first
+      // scores there; long tiles and d = 128 keep the plain loop (the restructured one
+      // measured 2-3 % slower on long tiles, where a tile boundary is rare).
+      if constexpr (kAhead) {
+        uint32_t s = 0;
+        int it = 0;
+        bool ok = true;
+        int tile = take_tile(0, 0x50f);
+        bool first_issued = false;   // this tile's first scores went out during the previous tile's last step
+        for (;; ++it) {
+          if (tile < 0) break;
+          int kb, bh;
+          group_order(tile, BHkv, nb, hg, kb, bh);
+          const int kvb = it % C::kKVBufs;
+          const int q0 = CAUSAL ? kb : 0;
+          const int nsteps = SPARSE ? sparse_n(kb) : group * (nb - q0);
+          if (!wait_warp(bar(C::kKVFull + kvb), (it / C::kKVBufs) & 1, ctl, 0x501)) break;
+          const uint32_t kbase = smem_u32(smem + C::kOffK + kvb * C::kTileBytes);
+          const uint32_t vbase = smem_u32(smem + C::kOffV + kvb * C::kTileBytes);
+          // first block of the tile
+          if (!first_issued) {
+            if (!wait_warp(bar(C::kQFull + s % C::kQBufs), (s / C::kQBufs) & 1, ctl, 0x502) ||
+                (s > 0 && !wait_warp(bar(C::kSTFree), (s - 1) & 1, ctl, 0x503)) ||
+                (!C::kEarly && s > 0 && !wait_warp(bar(C::kDQFree), (s - 1) & 1, ctl, 0x504))) {
               ok = false;
               break;
             }
             tc_fence_after();
             if (elect_one()) {
-              issue_st(kbase, qaddr(s + 1));
-              issue_fold_s(s + 1);
-              issue_dpt(vbase, oaddr(s + 1));
-              issue_fold_dp(s + 1);
+              issue_st(kbase, qaddr(s));
+              issue_fold_s(s);
+              issue_dpt(vbase, oaddr(s));
+              issue_fold_dp(s);
               umma_commit(bar(C::kSFull));
             }
             __syncwarp();
           }
-          if (!wait_warp(bar(C::kDSFull), s & 1, ctl, 0x507) ||
-              (i == 0 && it > 0 && !wait_warp(bar(C::kDKVEmpty), (it - 1) & 1, ctl, 0x508))) {
+          first_issued = false;
+          int next_tile = -2;   // taken during the last step
+          for (int i = 0; i < nsteps; ++i, ++s) {
+            const bool last = (i == nsteps - 1);
+            if (kAhead && last) {
+              // the next tile's first S^T and dP^T now, ahead of this block's gradients, when its
+              // K/V and first Q/dO have landed (the producer loaded them a tile ahead)
+              next_tile = take_tile(it + 1, 0x50e);
+              if (next_tile >= 0) {
+                const int kvn = (it + 1) % C::kKVBufs;
+                const bool ready =
+                    __all_sync(0xffffffffu, mbar_test(bar(C::kKVFull + kvn), ((it + 1) / C::kKVBufs) & 1) != 0u &&
+                                                mbar_test(bar(C::kQFull + (s + 1) % C::kQBufs),
+                                                              ((s + 1) / C::kQBufs) & 1) != 0u);
+                if (ready) {
+                  if (!wait_warp(bar(C::kSTFree), s & 1, ctl, 0x50d)) {
+                    ok = false;
+                    break;
+                  }
+                  tc_fence_after();
+                  if (elect_one()) {
+                    issue_st(smem_u32(smem + C::kOffK + kvn * C::kTileBytes), qaddr(s + 1));
+                    issue_fold_s(s + 1);
+                    issue_dpt(smem_u32(smem + C::kOffV + kvn * C::kTileBytes), oaddr(s + 1));
+                    issue_fold_dp(s + 1);
+                    umma_commit(bar(C::kSFull));
+                  }
+                  __syncwarp();
+                  first_issued = true;
+                }
+              }
+            }
+            if (C::kEarly && !last) {
+              if (!wait_warp(bar(C::kQFull + (s + 1) % C::kQBufs), ((s + 1) / C::kQBufs) & 1, ctl, 0x505) ||
+                  !wait_warp(bar(C::kSTFree), s & 1, ctl, 0x506)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              if (elect_one()) {
+                issue_st(kbase, qaddr(s + 1));
+                issue_fold_s(s + 1);
+                issue_dpt(vbase, oaddr(s + 1));
+                issue_fold_dp(s + 1);
+                umma_commit(bar(C::kSFull));
+              }
+              __syncwarp();
+            }
+            if (!wait_warp(bar(C::kDSFull), s & 1, ctl, 0x507) ||
+                (i == 0 && it > 0 && !wait_warp(bar(C::kDKVEmpty), (it - 1) & 1, ctl, 0x508))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            if (elect_one()) {
+              const uint32_t qbase = qaddr(s), obase = oaddr(s);
+              const uint64_t dsk = sdesc_sw128(dst, 16, 1024);                 // dS^T, K-major (A of dK)
+              const uint64_t omn = sdesc_sw128(obase, kChunkBytes, 1024);      // dO, MN-major (B of dV)
+              const uint64_t qmn = sdesc_sw128(qbase, kChunkBytes, 1024);      // Q, MN-major (B of dK)
+  #pragma unroll
+              for (int kk = 0; kk < kRows / 16; ++kk) {
+                const uint32_t acc = (i == 0 && kk == 0) ? 0u : 1u;
+                const uint32_t rows16 = (kk * 16 * 128) >> 4;                  // 16 rows of 128 bytes
+                // dV += P^T dO: A = P^T from tensor memory (16 query columns = 8 packed columns)
+                umma_ts(tmem + C::kTmDV, tmem + C::tm_pt(kk >> 2) + (kk & 3) * 8, omn + rows16, idesc_kv, acc);
+                // dK += dS^T Q: A = dS^T (keys x q, q contiguous), K-major, 16 q = 32 bytes
+                const uint32_t aoff = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
+                umma_ss(tmem + C::kTmDK, dsk + aoff, qmn + rows16, idesc_kv, acc);
+              }
+              // d = 128 (one Q/dO buffer): dV and dK are the last readers of this block's Q
+              // and dO, so the producer may refill the buffer while dQ (which reads dS and K)
+              // still runs.  (At d = 64, with three buffers, the earlier refill only competes
+              // with dQ and measured slower.)
+              if constexpr (!C::kEarly) umma_commit(bar(C::kQEmpty + s % C::kQBufs));
+              // d = 64: dK and dV are final after the tile's last dV and dK products: hand their
+              // columns to the read-out now, not after the last dQ product
+              if (kAhead && last) umma_commit(bar(C::kDKVFull));
+            }
+            __syncwarp();
+            // d = 64: dQ has its own columns, which the dQ warpgroup must have read out for
+            // the previous block; dV and dK above did not wait for that (at a tile's first
+            // block the same warpgroup is also writing the previous tile's dK and dV)
+            if (C::kEarly && s > 0 && !wait_warp(bar(C::kDQFree), (s - 1) & 1, ctl, 0x509)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            if (elect_one()) {
+              const uint64_t dsmn = sdesc_sw128(dst, kChunkBytes, 1024);       // dS, MN-major (A of dQ)
+              const uint64_t kmn = sdesc_sw128(kbase, kChunkBytes, 1024);      // K, MN-major (B of dQ)
+  #pragma unroll
+              for (int kk = 0; kk < kRows / 16; ++kk) {
+                // dQ = dS K: A = dS (q x keys) read MN-major from the dS^T block; B = K MN-major
+                const uint32_t rows16 = (kk * 16 * 128) >> 4;
+                umma_ss(tmem + C::kTmDQ, dsmn + rows16, kmn + rows16, idesc_q, kk > 0 ? 1u : 0u);
+              }
+              umma_commit(bar(C::kMmaDone));
+              if constexpr (C::kEarly) umma_commit(bar(C::kQEmpty + s % C::kQBufs));
+              umma_commit(bar(C::kDQFull));
+            }
+            __syncwarp();
+            if (!C::kEarly && !last) {
+              // S^T(next) overwrites the S^T columns that P^T(this) shared; tcgen05.mma
+              // from one thread run in issue order, so dV above has read P^T first.
+              if (!wait_warp(bar(C::kQFull + (s + 1) % C::kQBufs), ((s + 1) / C::kQBufs) & 1, ctl, 0x50a) ||
+                  !wait_warp(bar(C::kSTFree), s & 1, ctl, 0x50b)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              if (elect_one()) {
+                issue_st(kbase, qaddr(s + 1));
+                issue_fold_s(s + 1);
+              }
+              __syncwarp();
+              // dP^T(next) overwrites the dP^T columns that dQ(this) occupies
+              if (!wait_warp(bar(C::kDQFree), s & 1, ctl, 0x50c)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              if (elect_one()) {
+                issue_dpt(vbase, oaddr(s + 1));
+                issue_fold_dp(s + 1);
+                umma_commit(bar(C::kSFull));
+              }
+              __syncwarp();
+            }
+          }
+          if (!ok) break;
+          if (elect_one()) {
+            umma_commit(bar(C::kKVEmpty + kvb));
+            if constexpr (!kAhead) umma_commit(bar(C::kDKVFull));
+          }
+          __syncwarp();
+          tile = next_tile != -2 ? next_tile : take_tile(it + 1, 0x50f);
+        }
+      } else {
+        uint32_t s = 0;
+        int it = 0;
+        bool ok = true;
+        for (;; ++it) {
+          const int tile = take_tile(it, 0x50f);
+          if (tile < 0) break;
+          int kb, bh;
+          group_order(tile, BHkv, nb, hg, kb, bh);
+          const int kvb = it % C::kKVBufs;
+          const int q0 = CAUSAL ? kb : 0;
+          const int nsteps = SPARSE ? sparse_n(kb) : group * (nb - q0);
+          if (!wait_warp(bar(C::kKVFull + kvb), (it / C::kKVBufs) & 1, ctl, 0x501)) break;
+          const uint32_t kbase = smem_u32(smem + C::kOffK + kvb * C::kTileBytes);
+          const uint32_t vbase = smem_u32(smem + C::kOffV + kvb * C::kTileBytes);
+          // first block of the tile
+          if (!wait_warp(bar(C::kQFull + s % C::kQBufs), (s / C::kQBufs) & 1, ctl, 0x502) ||
+              (s > 0 && !wait_warp(bar(C::kSTFree), (s - 1) & 1, ctl, 0x503)) ||
+              (!C::kEarly && s > 0 && !wait_warp(bar(C::kDQFree), (s - 1) & 1, ctl, 0x504))) {
             ok = false;
             break;
           }
           tc_fence_after();
           if (elect_one()) {
-            const uint32_t qbase = qaddr(s), obase = oaddr(s);
-            const uint64_t dsk = sdesc_sw128(dst, 16, 1024);                 // dS^T, K-major (A of dK)
-            const uint64_t omn = sdesc_sw128(obase, kChunkBytes, 1024);      // dO, MN-major (B of dV)
-            const uint64_t qmn = sdesc_sw128(qbase, kChunkBytes, 1024);      // Q, MN-major (B of dK)
-#pragma unroll
-            for (int kk = 0; kk < kRows / 16; ++kk) {
-              const uint32_t acc = (i == 0 && kk == 0) ? 0u : 1u;
-              const uint32_t rows16 = (kk * 16 * 128) >> 4;                  // 16 rows of 128 bytes
-              // dV += P^T dO: A = P^T from tensor memory (16 query columns = 8 packed columns)
-              umma_ts(tmem + C::kTmDV, tmem + C::tm_pt(kk >> 2) + (kk & 3) * 8, omn + rows16, idesc_kv, acc);
-              // dK += dS^T Q: A = dS^T (keys x q, q contiguous), K-major, 16 q = 32 bytes
-              const uint32_t aoff = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-              umma_ss(tmem + C::kTmDK, dsk + aoff, qmn + rows16, idesc_kv, acc);
-            }
-            // d = 128 (one Q/dO buffer): dV and dK are the last readers of this block's Q
-            // and dO, so the producer may refill the buffer while dQ (which reads dS and K)
-            // still runs.  (At d = 64, with three buffers, the earlier refill only competes
-            // with dQ and measured slower.)
-            if constexpr (!C::kEarly) umma_commit(bar(C::kQEmpty + s % C::kQBufs));
+            issue_st(kbase, qaddr(s));
+            issue_fold_s(s);
+            issue_dpt(vbase, oaddr(s));
+            issue_fold_dp(s);
+            umma_commit(bar(C::kSFull));
           }
           __syncwarp();
-          // d = 64: dQ has its own columns, which the dQ warpgroup must have read out for
-          // the previous block; dV and dK above did not wait for that (at a tile's first
-          // block the same warpgroup is also writing the previous tile's dK and dV)
-          if (C::kEarly && s > 0 && !wait_warp(bar(C::kDQFree), (s - 1) & 1, ctl, 0x509)) {
-            ok = false;
-            break;
+          for (int i = 0; i < nsteps; ++i, ++s) {
+            const bool last = (i == nsteps - 1);
+            if (C::kEarly && !last) {
+              if (!wait_warp(bar(C::kQFull + (s + 1) % C::kQBufs), ((s + 1) / C::kQBufs) & 1, ctl, 0x505) ||
+                  !wait_warp(bar(C::kSTFree), s & 1, ctl, 0x506)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              if (elect_one()) {
+                issue_st(kbase, qaddr(s + 1));
+                issue_fold_s(s + 1);
+                issue_dpt(vbase, oaddr(s + 1));
+                issue_fold_dp(s + 1);
+                umma_commit(bar(C::kSFull));
+              }
+              __syncwarp();
+            }
+            if (!wait_warp(bar(C::kDSFull), s & 1, ctl, 0x507) ||
+                (i == 0 && it > 0 && !wait_warp(bar(C::kDKVEmpty), (it - 1) & 1, ctl, 0x508))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            if (elect_one()) {
+              const uint32_t qbase = qaddr(s), obase = oaddr(s);
+              const uint64_t dsk = sdesc_sw128(dst, 16, 1024);                 // dS^T, K-major (A of dK)
+              const uint64_t omn = sdesc_sw128(obase, kChunkBytes, 1024);      // dO, MN-major (B of dV)
+              const uint64_t qmn = sdesc_sw128(qbase, kChunkBytes, 1024);      // Q, MN-major (B of dK)
+  #pragma unroll
+              for (int kk = 0; kk < kRows / 16; ++kk) {
+                const uint32_t acc = (i == 0 && kk == 0) ? 0u : 1u;
+                const uint32_t rows16 = (kk * 16 * 128) >> 4;                  // 16 rows of 128 bytes
+                // dV += P^T dO: A = P^T from tensor memory (16 query columns = 8 packed columns)
+                umma_ts(tmem + C::kTmDV, tmem + C::tm_pt(kk >> 2) + (kk & 3) * 8, omn + rows16, idesc_kv, acc);
+                // dK += dS^T Q: A = dS^T (keys x q, q contiguous), K-major, 16 q = 32 bytes
+                const uint32_t aoff = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
+                umma_ss(tmem + C::kTmDK, dsk + aoff, qmn + rows16, idesc_kv, acc);
+              }
+              // d = 128 (one Q/dO buffer): dV and dK are the last readers of this block's Q
+              // and dO, so the producer may refill the buffer while dQ (which reads dS and K)
+              // still runs.  (At d = 64, with three buffers, the earlier refill only competes
+              // with dQ and measured slower.)
+              if constexpr (!C::kEarly) umma_commit(bar(C::kQEmpty + s % C::kQBufs));
+            }
+            __syncwarp();
+            // d = 64: dQ has its own columns, which the dQ warpgroup must have read out for
+            // the previous block; dV and dK above did not wait for that (at a tile's first
+            // block the same warpgroup is also writing the previous tile's dK and dV)
+            if (C::kEarly && s > 0 && !wait_warp(bar(C::kDQFree), (s - 1) & 1, ctl, 0x509)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            if (elect_one()) {
+              const uint64_t dsmn = sdesc_sw128(dst, kChunkBytes, 1024);       // dS, MN-major (A of dQ)
+              const uint64_t kmn = sdesc_sw128(kbase, kChunkBytes, 1024);      // K, MN-major (B of dQ)
+  #pragma unroll
+              for (int kk = 0; kk < kRows / 16; ++kk) {
+                // dQ = dS K: A = dS (q x keys) read MN-major from the dS^T block; B = K MN-major
+                const uint32_t rows16 = (kk * 16 * 128) >> 4;
+                umma_ss(tmem + C::kTmDQ, dsmn + rows16, kmn + rows16, idesc_q, kk > 0 ? 1u : 0u);
+              }
+              umma_commit(bar(C::kMmaDone));
+              if constexpr (C::kEarly) umma_commit(bar(C::kQEmpty + s % C::kQBufs));
+              umma_commit(bar(C::kDQFull));
+            }
+            __syncwarp();
+            if (!C::kEarly && !last) {
+              // S^T(next) overwrites the S^T columns that P^T(this) shared; tcgen05.mma
+              // from one thread run in issue order, so dV above has read P^T first.
+              if (!wait_warp(bar(C::kQFull + (s + 1) % C::kQBufs), ((s + 1) / C::kQBufs) & 1, ctl, 0x50a) ||
+                  !wait_warp(bar(C::kSTFree), s & 1, ctl, 0x50b)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              if (elect_one()) {
+                issue_st(kbase, qaddr(s + 1));
+                issue_fold_s(s + 1);
+              }
+              __syncwarp();
+              // dP^T(next) overwrites the dP^T columns that dQ(this) occupies
+              if (!wait_warp(bar(C::kDQFree), s & 1, ctl, 0x50c)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              if (elect_one()) {
+                issue_dpt(vbase, oaddr(s + 1));
+                issue_fold_dp(s + 1);
+                umma_commit(bar(C::kSFull));
+              }
+              __syncwarp();
+            }
           }
-          tc_fence_after();
+          if (!ok) break;
           if (elect_one()) {
-            const uint64_t dsmn = sdesc_sw128(dst, kChunkBytes, 1024);       // dS, MN-major (A of dQ)
-            const uint64_t kmn = sdesc_sw128(kbase, kChunkBytes, 1024);      // K, MN-major (B of dQ)
-#pragma unroll
-            for (int kk = 0; kk < kRows / 16; ++kk) {
-              // dQ = dS K: A = dS (q x keys) read MN-major from the dS^T block; B = K MN-major
-              const uint32_t rows16 = (kk * 16 * 128) >> 4;
-              umma_ss(tmem + C::kTmDQ, dsmn + rows16, kmn + rows16, idesc_q, kk > 0 ? 1u : 0u);
-            }
-            umma_commit(bar(C::kMmaDone));
-            if constexpr (C::kEarly) umma_commit(bar(C::kQEmpty + s % C::kQBufs));
-            umma_commit(bar(C::kDQFull));
+            umma_commit(bar(C::kKVEmpty + kvb));
+            umma_commit(bar(C::kDKVFull));
           }
           __syncwarp();
-          if (!C::kEarly && !last) {
-            // S^T(next) overwrites the S^T columns that P^T(this) shared; tcgen05.mma
-            // from one thread run in issue order, so dV above has read P^T first.
-            if (!wait_warp(bar(C::kQFull + (s + 1) % C::kQBufs), ((s + 1) / C::kQBufs) & 1, ctl, 0x50a) ||
-                !wait_warp(bar(C::kSTFree), s & 1, ctl, 0x50b)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            if (elect_one()) {
-              issue_st(kbase, qaddr(s + 1));
-              issue_fold_s(s + 1);
-            }
-            __syncwarp();
-            // dP^T(next) overwrites the dP^T columns that dQ(this) occupies
-            if (!wait_warp(bar(C::kDQFree), s & 1, ctl, 0x50c)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            if (elect_one()) {
-              issue_dpt(vbase, oaddr(s + 1));
-              issue_fold_dp(s + 1);
-              umma_commit(bar(C::kSFull));
-            }
-            __syncwarp();
-          }
         }
-        if (!ok) break;
-        if (elect_one()) {
-          umma_commit(bar(C::kKVEmpty + kvb));
-          umma_commit(bar(C::kDKVFull));
-        }
-        __syncwarp();
       }
       if (elect_one()) umma_commit(bar(C::kDrain));
       __syncwarp();
@@ -695,14 +976,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int g = 0; ok && g < group; ++g) {
       const int bhq = first_q_head(bh) + g;
       for (int qi = q0, j = 0; SPARSE ? j < nq : qi < nb; ++s, ++j, qi = SPARSE ? sparse_q(kb, j) : qi + 1) {
+        const bool tile_last = g == group - 1 && (SPARSE ? j == nq - 1 : qi == nb - 1);
+        // short d = 64 tiles: dK and dV are handed over after the tile's last dV and dK
+        // products, before its last dQ product: they are read out first
+        if (kAhead && tile_last && !write_dkdv(it, kb, bh)) {
+          ok = false;
+          break;
+        }
         if (!wait_warp(bar(C::kDQFull), s & 1, ctl, 0x701)) {
           ok = false;
           break;
         }
-        // d = 64: the next tile's first gradient MMAs wait for the dK/dV columns, so
-        // those are read out before the last dQ of the tile (at d = 128 the next
-        // tile's first scores wait for the dQ columns instead, so dQ goes first)
-        if (C::kEarly && g == group - 1 && (SPARSE ? j == nq - 1 : qi == nb - 1) && !write_dkdv(it, kb, bh)) {
+        // long d = 64 tiles: the next tile's first gradient MMAs wait for the dK/dV columns,
+        // so those are read out before the last dQ of the tile (at d = 128 the next tile's
+        // first scores wait for the dQ columns instead, so dQ goes first)
+        if (C::kEarly && !kAhead && tile_last && !write_dkdv(it, kb, bh)) {
           ok = false;
           break;
         }

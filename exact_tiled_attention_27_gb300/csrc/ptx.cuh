@@ -111,6 +111,19 @@ struct WaitCtl {
   uint64_t limit_ns;            // wait limit
 };
 
+// Non-blocking test of the phase with parity `parity` of the mbarrier at `bar` (no suspend).
+__device__ __forceinline__ uint32_t mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok;
+}
+
 // Bounded wait for the phase with parity `parity` of the mbarrier at `bar`.
 // Returns true when the phase completed; false when this CTA is aborting (this
 // wait gave up after ctl.limit_ns, or another thread of the CTA already did).
